@@ -1,0 +1,240 @@
+"""CPU oracle for the owner-local optimizer step (TEST INFRASTRUCTURE ONLY).
+
+Only the test-suite, the smoke check and the benchmark's CPU-baseline leg may
+import this module. The library never calls it, and it shares no code with the
+CUDA path: it is plain NumPy in float64, written to be checked by eye against
+the pages it cites.
+
+Sources (cited by page title and section):
+  [MFSDP]  "MatrixFSDP: communication-free matrix optimizers under ZeRO-3
+           parameter sharding" (arXiv 2607.05895v1).
+           Section 3 (owner placement: the owner runs Muon on the whole 2D
+           matrix, the tail owner runs AdamW), section 4.4 (optimizer routing),
+           section 5.1 (hyperparameters: Muon lr 1e-3, wd 1e-2; AdamW betas,
+           eps 1e-8, decoupled weight decay as in Loshchilov and Hutter).
+  [SHARD]  "Optimizers In A Sharded World: Muon's O(mn) Vs RMNP's Zero".
+           Section 1 (momentum V_t = mu V_{t-1} + G_t; Muon's target direction
+           (V V^T)^{-1/2} V approximated by five Newton-Schulz iterations of
+           three products each; RMNP direction V_i / ||V_i||_2 per row), and
+           the appendix "The Code That Ran" (the quintic iteration with
+           coefficients (3.4445, -4.7750, 2.0315) and eps 1e-7 added to the
+           Frobenius norm, the transpose when rows > cols, the shape scale
+           sqrt(max(1, rows/cols)), the row-normalisation with fp32 sums and
+           the 1e-12 clamp of F.normalize).
+
+Readings where the pages are silent (each also listed in the design notes):
+  * The iteration is written as A = X X^T, B = b A + c A A, X' = a X + B X.
+    The appendix script writes it as A = X X^T, B = A X, X' = a X + b B + c A B;
+    the two are equal in exact arithmetic (a self-check pins this).
+  * The Frobenius norm is taken of the fp32 momentum; X0 = bf16(V / (||V|| + eps)).
+  * Weight decay is decoupled and multiplicative for Muon and RMNP, with the
+    same learning rate: W <- W (1 - lr wd) - lr s D.
+  * The last iterate is not rounded to bf16 before the weight update.
+  * AdamW: bias-corrected moments, eps outside the square root, step t >= 1.
+
+bf16 emulation: with `round_bf16=True` every matrix the GPU stores in bf16 as a
+GEMM operand (X between iterations, A and B) is rounded to nearest-even bf16
+directly from float64; accumulation stays float64.
+
+Parity status: every function below is pinned by the CPU tests against
+closed forms, library routines or invariants; none is unpinned.
+"""
+from __future__ import annotations
+
+import math
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+# default quintic coefficients ([SHARD] appendix)
+NS_COEFFS = (3.4445, -4.7750, 2.0315)
+NS_EPS = 1e-7            # added to the Frobenius norm ([SHARD] appendix)
+RMNP_EPS = 1e-12         # F.normalize clamp ([SHARD] appendix, row-sharded RMNP)
+
+_BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+_BF16_MIN_QUANTUM_EXP = -133   # quantum of bf16 subnormals: 2^-126 * 2^-7
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding
+# ---------------------------------------------------------------------------
+
+def bf16_round(x) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value (ties to even), returned
+    as float64. bf16 keeps 8 significant bits, the fp32 exponent range and
+    gradual underflow; values beyond the largest finite bf16 become +-inf."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.array(x, dtype=np.float64, copy=True)
+    fin = np.isfinite(x)
+    xf = x[fin]
+    _, e = np.frexp(xf)                      # xf = f * 2^e with 0.5 <= |f| < 1
+    q = np.maximum(e - 8, _BF16_MIN_QUANTUM_EXP)
+    y = np.ldexp(np.rint(np.ldexp(xf, -q)), q)   # np.rint rounds halves to even
+    y = np.where(np.abs(y) > _BF16_MAX, np.copysign(np.inf, xf), y)
+    out[fin] = y
+    return out
+
+
+def _identity(x):
+    return x
+
+
+# ---------------------------------------------------------------------------
+# Muon ([SHARD] section 1 and appendix; [MFSDP] sections 3, 4.4)
+# ---------------------------------------------------------------------------
+
+def momentum(V: np.ndarray, G: np.ndarray, mu: float) -> np.ndarray:
+    """Heavy-ball momentum V_t = mu V_{t-1} + G_t ([SHARD] section 1)."""
+    return mu * np.asarray(V, np.float64) + np.asarray(G, np.float64)
+
+
+def frobenius_normalize(V: np.ndarray, eps: float = NS_EPS) -> np.ndarray:
+    """X = V / (||V||_F + eps) ([SHARD] appendix, first lines of the quintic
+    iteration)."""
+    V = np.asarray(V, np.float64)
+    return V / (math.sqrt(float(np.sum(V * V))) + eps)
+
+
+def newton_schulz(X0: np.ndarray, coeffs: Sequence[float] = NS_COEFFS, steps: int = 5,
+                  round_bf16: bool = False, trace: Optional[list] = None) -> np.ndarray:
+    """Quintic Newton-Schulz iteration ([SHARD] section 1: five iterations of
+    three matrix products approximating (X X^T)^{-1/2} X; appendix: the
+    coefficients and the transpose to the wide orientation).
+
+    X0 is already normalised. If X0 has more rows than columns the iteration
+    runs on X0^T and the result is transposed back. Per iteration:
+        A  = X X^T
+        B  = b A + c A A
+        X' = a X + B X
+    With round_bf16, X (before every iteration), A and B are rounded to bf16;
+    the final iterate is returned unrounded. `trace`, if given, receives
+    (name, array) pairs of every stored intermediate."""
+    a, b, c = (float(t) for t in coeffs)
+    q = bf16_round if round_bf16 else _identity
+    X = np.asarray(X0, np.float64)
+    tall = X.shape[0] > X.shape[1]
+    if tall:
+        X = X.T
+    X = q(X)
+    if trace is not None:
+        trace.append(("X0", X))
+    for k in range(steps):
+        A = q(X @ X.T)
+        B = q(b * A + c * (A @ A))
+        Xn = a * X + B @ X
+        X = q(Xn) if k < steps - 1 else Xn
+        if trace is not None:
+            trace.extend([(f"A{k}", A), (f"B{k}", B), (f"X{k + 1}", X)])
+    return X.T if tall else X
+
+
+def newton_schulz_pages_form(X0: np.ndarray, coeffs: Sequence[float] = NS_COEFFS,
+                             steps: int = 5) -> np.ndarray:
+    """The same iteration in the algebraic form of the appendix script:
+    A = X X^T, B = A X, X' = a X + b B + c A B (no rounding). Used only to
+    check that the two forms agree."""
+    a, b, c = (float(t) for t in coeffs)
+    X = np.asarray(X0, np.float64)
+    tall = X.shape[0] > X.shape[1]
+    if tall:
+        X = X.T
+    for _ in range(steps):
+        A = X @ X.T
+        B = A @ X
+        X = a * X + b * B + c * (A @ B)
+    return X.T if tall else X
+
+
+def shape_scale(rows: int, cols: int) -> float:
+    """sqrt(max(1, rows/cols)) on the stored [out, in] shape ([SHARD]
+    appendix, scale of the Muon and RMNP updates)."""
+    return math.sqrt(max(1.0, rows / cols))
+
+
+def decoupled_update(W: np.ndarray, D: np.ndarray, lr: float, wd: float, scale: float) -> np.ndarray:
+    """W <- W (1 - lr wd) - lr scale D (decoupled weight decay, [MFSDP]
+    section 5.1 gives wd; the multiplicative form is the reading taken)."""
+    return np.asarray(W, np.float64) * (1.0 - lr * wd) - (lr * scale) * np.asarray(D, np.float64)
+
+
+def muon_matrix_step(W, G, V, lr=0.02, wd=0.01, mu=0.95, coeffs=NS_COEFFS, eps=NS_EPS,
+                     ns_steps=5, round_bf16=True):
+    """One owner-local Muon step on a whole 2D matrix ([MFSDP] section 3: the
+    owner holds the full gradient; [SHARD] section 1 and appendix for the
+    arithmetic). Returns (W_new, V_new, O) where O is the Newton-Schulz output
+    in the stored orientation."""
+    R, C = np.shape(W)
+    Vn = momentum(V, G, mu)
+    X0 = frobenius_normalize(Vn, eps)
+    O = newton_schulz(X0, coeffs, ns_steps, round_bf16=round_bf16)
+    Wn = decoupled_update(W, O, lr, wd, shape_scale(R, C))
+    return Wn, Vn, O
+
+
+# ---------------------------------------------------------------------------
+# RMNP ([SHARD] sections 1 and 5, appendix rmnp_local)
+# ---------------------------------------------------------------------------
+
+def rmnp_direction(V: np.ndarray, eps: float = RMNP_EPS) -> np.ndarray:
+    """D_i = V_i / max(||V_i||_2, eps) for every stored row i ([SHARD]
+    section 1; the clamp is F.normalize's, as used in the appendix)."""
+    V = np.asarray(V, np.float64)
+    norms = np.sqrt(np.sum(V * V, axis=1))
+    return V / np.maximum(norms, eps)[:, None]
+
+
+def rmnp_matrix_step(W, G, V, lr=0.02, wd=0.01, mu=0.95, eps=RMNP_EPS):
+    """One RMNP step: momentum, row normalisation, shape-scaled decoupled
+    update. Returns (W_new, V_new, D)."""
+    R, C = np.shape(W)
+    Vn = momentum(V, G, mu)
+    D = rmnp_direction(Vn, eps)
+    Wn = decoupled_update(W, D, lr, wd, shape_scale(R, C))
+    return Wn, Vn, D
+
+
+def rmnp_row_sharded(V: np.ndarray, shards: int, eps: float = RMNP_EPS) -> np.ndarray:
+    """RMNP computed shard by shard over contiguous row blocks and
+    concatenated ([SHARD] section 5: each rank normalises its own complete
+    rows)."""
+    V = np.asarray(V, np.float64)
+    m = V.shape[0]
+    parts = [rmnp_direction(V[r * m // shards:(r + 1) * m // shards], eps) for r in range(shards)]
+    return np.concatenate(parts, axis=0)
+
+
+# ---------------------------------------------------------------------------
+# AdamW on the packed non-matrix tail ([MFSDP] sections 3, 4.4, 5.1)
+# ---------------------------------------------------------------------------
+
+def adamw_step(p, g, m, v, lr=1e-3, wd=1e-2, beta1=0.9, beta2=0.95, eps=1e-8, step=1):
+    """Decoupled AdamW with bias correction (the tail owner's optimizer,
+    [MFSDP] section 3; hyperparameters section 5.1). `step` is t after the
+    increment (t >= 1). Returns (p_new, m_new, v_new)."""
+    if step < 1:
+        raise ValueError("step must be >= 1")
+    p = np.asarray(p, np.float64)
+    g = np.asarray(g, np.float64)
+    m = np.asarray(m, np.float64)
+    v = np.asarray(v, np.float64)
+    p = p * (1.0 - lr * wd)
+    m = beta1 * m + (1.0 - beta1) * g
+    v = beta2 * v + (1.0 - beta2) * g * g
+    m_hat = m / (1.0 - beta1 ** step)
+    v_hat = v / (1.0 - beta2 ** step)
+    p = p - lr * m_hat / (np.sqrt(v_hat) + eps)
+    return p, m, v
+
+
+# ---------------------------------------------------------------------------
+# whole-table helpers
+# ---------------------------------------------------------------------------
+
+def muon_table_step(mats: List[Tuple[np.ndarray, np.ndarray, np.ndarray]], **kw):
+    """Muon over an owner's shape table: the matrices are independent, so the
+    table step is the per-matrix step applied to each ([MFSDP] section 4.4)."""
+    return [muon_matrix_step(W, G, V, **kw) for (W, G, V) in mats]
+
+
+def rmnp_table_step(mats, **kw):
+    return [rmnp_matrix_step(W, G, V, **kw) for (W, G, V) in mats]
