@@ -1,0 +1,447 @@
+"""Benchmark of the owner-local optimizer step on GB300.
+
+One step = the whole hot path over one owner's table: the Muon step on every
+2D matrix (momentum, Frobenius normalisation, five quintic Newton-Schulz
+iterations, shape-scaled update with weight decay), AdamW on the packed
+non-matrix tail, and RMNP on the same matrices (its own momentum and weight
+copies). Default workload: the GPT-2 Large matrix set (144 matrices, 707.8 M
+elements; tail 601,600 elements), synthetic seeded inputs resident in HBM.
+The working set (~17 GB) is far larger than L2, so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
+independent replica of the workload on its own GPU (the step has no exchange);
+the time is the max over ranks and the value is the sum of all ranks' work.
+`--impl reference` times the CPU oracle on the host cores instead (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "owner Muon step ms & NS TFLOP/s vs bf16 peak; RMNP/AdamW HBM GB/s"
+UNIT = "TFLOP/s"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if self.t0 is not None and self.t1 is not None and self.t0 - 0.06 <= ts <= self.t1 + 0.06]
+        use = inside if inside else [r for _, r in rows]
+        sm = [float(r[1]) for r in use if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in use for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_max": max((float(r[3]) for r in use if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def cpu_oracle_sample(wl, max_seconds=20.0, indices=None):
+    """Times the CPU oracle (as it stands) on a bounded sample of the
+    workload: whole-matrix Muon steps on one matrix per distinct shape, in
+    table order, until max_seconds is spent. Returns (TFLOP/s, seconds,
+    description, cores)."""
+    import numpy as np
+    import oracle
+    from matrix_optimizers_zero_gb300 import workloads
+    cores = len(os.sched_getaffinity(0))
+    seen, picks = set(), []
+    for i, s in enumerate(wl.matrices):
+        if (s.rows, s.cols) not in seen:
+            seen.add((s.rows, s.cols))
+            picks.append(i)
+    if indices is not None:
+        picks = indices
+    flops = 0
+    t_total = 0.0
+    done = []
+    for i in picks:
+        W, G, V = workloads.host_matrix(wl, i, v_std=1e-3)
+        W, G, V = (t.float().double().numpy() for t in (W, G, V))
+        t0 = time.perf_counter()
+        oracle.muon_matrix_step(W, G, V, lr=wl.lr, wd=wl.wd, mu=wl.mu, ns_steps=wl.ns_steps)
+        t_total += time.perf_counter() - t0
+        s = wl.matrices[i]
+        flops += workloads.ns_alg_flops(s.rows, s.cols, wl.ns_steps)
+        done.append(f"{s.rows}x{s.cols}")
+        if t_total > max_seconds:
+            break
+    desc = f"oracle muon_matrix_step (fp64 numpy, bf16 emulation) on {len(done)} matrices [{', '.join(done)}]"
+    return flops / t_total / 1e12, t_total, desc, cores
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import matrix_optimizers_zero_gb300 as mo
+    from matrix_optimizers_zero_gb300 import build as mo_build, workloads
+
+    mo_build.build()
+    mo.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = workloads.get_workload(args.config)
+    peaks = load_peaks()
+
+    # ---- state: flat device buffers with per-matrix views (one copy each for e2e)
+    shapes = [(s.rows, s.cols) for s in wl.matrices]
+    offs, tot = [], 0
+    for r, c in shapes:
+        offs.append(tot)
+        tot += ((r * c + 63) // 64) * 64
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    Wf = torch.randn(tot, generator=gen, device=dev).mul_(wl.w_std)
+    Gf = torch.randn(tot, generator=gen, device=dev).mul_(wl.g_std).to(torch.bfloat16)
+    Vf = torch.randn(tot, generator=gen, device=dev).mul_(1e-3)
+    Wr = Wf.clone()
+    Vr = Vf.clone()
+
+    def views(flat):
+        return [flat[o:o + r * c].view(r, c) for o, (r, c) in zip(offs, shapes)]
+
+    W_l, G_l, V_l, Wr_l, Vr_l = views(Wf), views(Gf), views(Vf), views(Wr), views(Vr)
+    muon_tbl = mo.MuonTable(list(zip(W_l, G_l, V_l)))
+    rmnp_tbl = mo.MuonTable(list(zip(Wr_l, G_l, Vr_l)))
+    tail_sizes = [t for t in wl.tail if t > 0]
+    toffs, ttot = [], 0
+    for t in tail_sizes:
+        toffs.append(ttot)
+        ttot += ((t + 63) // 64) * 64
+    Pf = torch.randn(max(ttot, 1), generator=gen, device=dev).mul_(wl.tail_p_std)
+    Tg = torch.randn(max(ttot, 1), generator=gen, device=dev).mul_(wl.tail_g_std)
+    Tm = torch.zeros(max(ttot, 1), device=dev)
+    Tv = torch.zeros(max(ttot, 1), device=dev)
+    segs = [(Pf[o:o + t], Tg[o:o + t], Tm[o:o + t], Tv[o:o + t]) for o, t in zip(toffs, tail_sizes)]
+    tail_tbl = mo.TailTable(segs)
+
+    mp = mo.MuonParams(lr=wl.lr, wd=wl.wd, mu=wl.mu, ns_steps=wl.ns_steps)
+    rp = mo.RmnpParams(lr=wl.lr, wd=wl.wd, mu=wl.mu)
+    ws = mo.muon_workspace(muon_tbl, mp, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    lib = mo.load_library()
+    import ctypes
+    ws_ptr, ws_bytes = ws.data_ptr(), ws.numel()
+    sptr = stream.cuda_stream
+    adam_step = [0]
+
+    def step(ev=None):
+        if ev is None:
+            st = lib.muon_owner_step(muon_tbl.ptr, muon_tbl.n, ctypes.byref(mp), ws_ptr, ws_bytes, sptr)
+        else:
+            ev[0].record(stream)
+            st = lib.muon_owner_step_timed(muon_tbl.ptr, muon_tbl.n, ctypes.byref(mp), ws_ptr, ws_bytes, sptr,
+                                           ev[1].cuda_event, ev[2].cuda_event)
+        if st != 0:
+            raise mo.MoError(st, "muon_owner_step")
+        if ev is not None:
+            ev[3].record(stream)
+        adam_step[0] += 1
+        ap = mo.AdamWParams(lr=wl.adam_lr, wd=wl.adam_wd, beta1=wl.beta1, beta2=wl.beta2, eps=wl.adam_eps,
+                            step=adam_step[0])
+        st = lib.adamw_tail_step(tail_tbl.ptr, tail_tbl.n, ctypes.byref(ap), sptr)
+        if st != 0:
+            raise mo.MoError(st, "adamw_tail_step")
+        if ev is not None:
+            ev[4].record(stream)
+        st = lib.rmnp_step(rmnp_tbl.ptr, rmnp_tbl.n, ctypes.byref(rp), sptr)
+        if st != 0:
+            raise mo.MoError(st, "rmnp_step")
+        if ev is not None:
+            ev[5].record(stream)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- warmup
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if mo.mo_last_device_error() != 0:
+        raise RuntimeError("device-side timeout during warmup")
+
+    # ---- timed region (kernel-level: inputs resident in HBM)
+    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    clocks.mark("begin")
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    barrier()
+    clocks.mark("end")
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    ms_step = total_ms / args.steps
+    pro_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ns_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    muon_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
+    adam_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+    rmnp_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in evs)
+
+    ns_flops = workloads.workload_alg_flops(wl)
+    ns_dense = sum(workloads.ns_dense_flops(r, c, wl.ns_steps) for r, c in shapes)
+    n_el = wl.n_elements
+    ns_tflops = ns_flops / (ns_ms * 1e-3) / 1e12
+    rmnp_gbs = n_el * workloads.RMNP_BYTES_PER_EL / (rmnp_ms * 1e-3) / 1e9
+    adam_gbs = wl.tail_elements * workloads.ADAMW_BYTES_PER_EL / (adam_ms * 1e-3) / 1e9
+    pro_gbs = n_el * 16 / (pro_ms * 1e-3) / 1e9
+
+    # max over ranks
+    t_rank = torch.tensor([ms_step], device=dev, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t_rank, op=dist.ReduceOp.MAX)
+    ms_max = float(t_rank.item())
+    value = world * ns_flops / (ms_max * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers
+    e2e_steps = max(1, min(args.steps, 10))
+    hG = torch.empty(Gf.numel(), dtype=torch.bfloat16, pin_memory=True)
+    hG.copy_(Gf)
+    hTg = torch.empty(Tg.numel(), dtype=torch.float32, pin_memory=True)
+    hTg.copy_(Tg)
+    hW = torch.empty(Wf.numel(), dtype=torch.float32, pin_memory=True)
+    hWr = torch.empty(Wr.numel(), dtype=torch.float32, pin_memory=True)
+    hP = torch.empty(Pf.numel(), dtype=torch.float32, pin_memory=True)
+    h2d = hG.numel() * 2 + hTg.numel() * 4
+    d2h = hW.numel() * 4 + hWr.numel() * 4 + hP.numel() * 4
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        Gf.copy_(hG, non_blocking=True)
+        Tg.copy_(hTg, non_blocking=True)
+        step()
+        hW.copy_(Wf, non_blocking=True)
+        hWr.copy_(Wr, non_blocking=True)
+        hP.copy_(Pf, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    t_e2e = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+    e2e_value = world * ns_flops / (float(t_e2e.item()) * 1e-3) / 1e12
+    if mo.mo_last_device_error() != 0:
+        raise RuntimeError("device-side timeout during the timed region")
+
+    if rank != 0:
+        return None
+
+    launches_per_step = (2 + 3 * wl.ns_steps) + math.ceil(len(tail_sizes) / 256) + math.ceil(len(shapes) / 512)
+    peak = peaks["bf16_tflops_sustained"]
+    out = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{wl.name}: {len(shapes)} matrices, {n_el} elements, tail {wl.tail_elements}",
+            "ns_steps": wl.ns_steps,
+            "step": "muon_owner_step + adamw_tail_step + rmnp_step",
+            "value_definition": "algorithmic Newton-Schulz flops 5(3m^2n+m^3) per matrix / whole-step time",
+            "l2": "inputs larger than L2 (no flush)",
+            "parallelism": f"replicas x{world}",
+            "state": "fp32 W/V, bf16 G; NS operands bf16 with fp32 accumulation",
+        },
+        "breakdown": {
+            "muon_step_ms": round(muon_ms, 4),
+            "prologue_ms": round(pro_ms, 4),
+            "prologue_gbs": round(pro_gbs, 1),
+            "ns_ms": round(ns_ms, 4),
+            "ns_tflops_alg": round(ns_tflops, 2),
+            "ns_tflops_dense_equiv": round(ns_dense / (ns_ms * 1e-3) / 1e12, 2),
+            "adamw_ms": round(adam_ms, 4),
+            "adamw_gbs": round(adam_gbs, 1),
+            "rmnp_ms": round(rmnp_ms, 4),
+            "rmnp_gbs": round(rmnp_gbs, 1),
+            "rmnp_frac_hbm": round(rmnp_gbs / peaks["hbm_gbs"], 4),
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "ns_gemm_kernel (Gram, A.A and B.X launches of all iterations)",
+            "achieved": round(ns_tflops, 2),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(ns_tflops / peak, 4),
+            "traffic": None,
+            "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
+        },
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(float(t_e2e.item()), 3)},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        v, secs, desc, cores = cpu_oracle_sample(wl, max_seconds=args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": desc, "seconds": round(secs, 2)}
+    return out
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    from matrix_optimizers_zero_gb300 import workloads
+    wl = workloads.get_workload(args.config)
+    seen, picks = set(), []
+    for i, s in enumerate(wl.matrices):
+        if (s.rows, s.cols) not in seen:
+            seen.add((s.rows, s.cols))
+            picks.append(i)
+    cores = len(os.sched_getaffinity(0))
+    for k in range(args.warmup):
+        cpu_oracle_sample(wl, max_seconds=0.0, indices=[picks[k % len(picks)]])
+    times, flops = [], 0
+    for k in range(args.steps):
+        i = picks[k % len(picks)]
+        v, secs, _, _ = cpu_oracle_sample(wl, max_seconds=0.0, indices=[i])
+        s = wl.matrices[i]
+        times.append(secs)
+        flops += workloads.ns_alg_flops(s.rows, s.cols, wl.ns_steps)
+    total = sum(times)
+    value = flops / total / 1e12
+    desc = (f"each step: the oracle's whole-matrix Muon step on one matrix of the {wl.name} table, cycling "
+            f"through its {len(picks)} distinct shapes")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name} (bounded sample per step)", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="gpt2l")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        out = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * mo.h -- C ABI of the GB300 (sm_103a) owner-local optimizer step.
+ *
+ * The library implements the optimizer step that owner placement makes local
+ * ("MatrixFSDP: communication-free matrix optimizers under ZeRO-3 parameter
+ * sharding", section 3 and section 4.4: the owner of a whole 2D matrix runs
+ * Muon on it; the tail owner runs AdamW on the packed non-matrix tensors), and
+ * the row-normalised alternative RMNP ("Optimizers In A Sharded World: Muon's
+ * O(mn) Vs RMNP's Zero", sections 1 and 5).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device, owned
+ *    by the caller. Tables (mo_matrix, mo_tail_seg) and parameter structs are
+ *    HOST memory, read during the call and not retained.
+ *  - Matrices are dense row-major [rows, cols] ([out, in]) with no padding.
+ *    Every base pointer must be 16-byte aligned.
+ *  - Work is enqueued on `stream` and is asynchronous; no call synchronises
+ *    the stream except mo_last_device_error. State (W, V, m, v) is updated
+ *    in place.
+ *  - Return value: MO_OK (0) or a negative MO_ERR_* code. Every argument is
+ *    validated before anything is enqueued, so a rejected call has no effect.
+ *    A failing CUDA runtime call yields MO_ERR_CUDA; mo_last_cuda_error()
+ *    returns its cudaError_t.
+ *  - A table with n == 0 is a no-op returning MO_OK.
+ *  - NaN/Inf in gradients propagate; they are not checked.
+ *  - Not thread-safe for concurrent calls that share a workspace.
+ */
+#ifndef MO_H_
+#define MO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MO_ABI_VERSION 1
+
+enum mo_status {
+  MO_OK = 0,
+  MO_ERR_NULL_POINTER = -1,      /* a required pointer is NULL */
+  MO_ERR_BAD_SHAPE = -2,         /* rows/cols/numel <= 0, n < 0, or a size over the supported maximum */
+  MO_ERR_MISALIGNED = -3,        /* a device pointer is not 16-byte aligned */
+  MO_ERR_BAD_PARAM = -4,         /* a hyperparameter is NaN/Inf or out of range */
+  MO_ERR_WORKSPACE_TOO_SMALL = -5,
+  MO_ERR_OVERLAP = -6,           /* W, V (or p, m, v) of one entry overlap */
+  MO_ERR_CUDA = -7,              /* a CUDA runtime call failed; see mo_last_cuda_error() */
+  MO_ERR_DEVICE_TIMEOUT = -8,    /* a bounded device-side wait expired (see mo_last_device_error) */
+  MO_ERR_UNSUPPORTED_DEVICE = -9 /* the current device is not sm_103 */
+};
+
+/* One 2D matrix of an owner's shape table ("MatrixFSDP", section 4.1: one
+ * full segment per matrix on its owner).
+ *   W    fp32 [rows, cols] master weight, updated in place
+ *   G    bf16 [rows, cols] gradient (bit pattern of bfloat16), read only
+ *   V    fp32 [rows, cols] momentum, updated in place
+ * W and V must not overlap; G may alias nothing that is written. */
+typedef struct {
+  float* W;
+  const void* G;
+  float* V;
+  int64_t rows;
+  int64_t cols;
+} mo_matrix;
+
+/* Muon hyperparameters ("Optimizers In A Sharded World", section 1 and the
+ * appendix benchmark script; "MatrixFSDP", section 5.1 for weight decay).
+ *   V <- mu V + G;  X0 = V / (||V||_F + eps), transposed if rows > cols;
+ *   ns_steps x { A = X X^T;  B = b A + c A A;  X = a X + B X };
+ *   W <- W (1 - lr wd) - lr sqrt(max(1, rows/cols)) X (transposed back).
+ * Defaults: lr 0.02, wd 0.01, mu 0.95, (a,b,c) = (3.4445, -4.7750, 2.0315),
+ * eps 1e-7, ns_steps 5. ns_steps must be in [1, 100]. */
+typedef struct {
+  float lr, wd, mu, a, b, c, eps;
+  int32_t ns_steps;
+} mo_muon_params;
+
+/* RMNP hyperparameters ("Optimizers In A Sharded World", section 1 and the
+ * appendix rmnp_local): V <- mu V + G; D_i = V_i / max(||V_i||_2, eps) per
+ * stored row; W <- W (1 - lr wd) - lr sqrt(max(1, rows/cols)) D.
+ * eps defaults to 1e-12. */
+typedef struct {
+  float lr, wd, mu, eps;
+} mo_rmnp_params;
+
+/* One packed segment of the non-matrix AdamW tail ("MatrixFSDP", section 3).
+ * p, g, m, v: fp32 [numel]; p, m, v updated in place, g read only. */
+typedef struct {
+  float* p;
+  const float* g;
+  float* m;
+  float* v;
+  int64_t numel;
+} mo_tail_seg;
+
+/* AdamW hyperparameters ("MatrixFSDP", section 5.1: decoupled weight decay).
+ * step is t AFTER the increment (t >= 1):
+ *   m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2;
+ *   p <- p (1 - lr wd) - lr (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps). */
+typedef struct {
+  float lr, wd, beta1, beta2, eps;
+  int64_t step;
+} mo_adamw_params;
+
+/* Bytes of device workspace muon_owner_step needs for this table. Host-only
+ * computation (no CUDA call). Returns 0 if the table or params are invalid. */
+size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_params* params);
+
+/* The Muon step over every matrix of the table, on `stream`.
+ * ws: device workspace of at least mo_muon_workspace_bytes() bytes, 256-byte
+ * aligned, owned by the caller; its contents are scratch, overwritten by every
+ * call (two calls in flight on different streams must not share it).
+ * Launches: one fused momentum + norm + bf16-cast prologue, then for each of
+ * the ns_steps iterations three grouped tcgen05 GEMM launches (Gram, A.A with
+ * the b A + c A A epilogue, B.X with the a X + epilogue); the last B.X launch
+ * applies the weight update in its epilogue. Matrices are independent. */
+int muon_owner_step(const mo_matrix* tbl, int32_t n, const mo_muon_params* params,
+                    void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* As muon_owner_step, and additionally records `ev_ns_begin` on the stream
+ * after the prologue (before the first GEMM launch) and `ev_ns_end` after the
+ * last GEMM launch, so the caller can time the Newton-Schulz part alone.
+ * Either event may be NULL. */
+int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params* params,
+                          void* ws, size_t ws_bytes, cudaStream_t stream,
+                          cudaEvent_t ev_ns_begin, cudaEvent_t ev_ns_end);
+
+/* AdamW over every tail segment, on `stream` (one grouped launch per 256
+ * segments). */
+int adamw_tail_step(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* params,
+                    cudaStream_t stream);
+
+/* RMNP over every matrix of the table, on `stream` (one grouped launch per 512
+ * matrices; no workspace). The shape scale is sqrt(max(1, rows/cols)) of each
+ * entry's own rows and cols. Rows are independent, so an entry may also be a
+ * contiguous row block of a larger matrix; use rmnp_step_scaled to give such
+ * blocks the whole matrix's scale. */
+int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cudaStream_t stream);
+
+/* RMNP with an explicit per-entry shape scale (scales[i] replaces
+ * sqrt(max(1, rows/cols)) for entry i), so that row blocks of one matrix can
+ * be updated with the whole matrix's scale ("Optimizers In A Sharded World",
+ * appendix rmnp_local: the scale uses the full matrix's rows). */
+int rmnp_step_scaled(const mo_matrix* tbl, const float* scales, int32_t n,
+                     const mo_rmnp_params* params, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device-side status word:
+ * MO_OK, or MO_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel expired
+ * (the kernel then skipped its remaining work and released its resources). */
+int mo_last_device_error(cudaStream_t stream);
+
+/* cudaError_t of the most recent MO_ERR_CUDA on this thread (0 if none). */
+int mo_last_cuda_error(void);
+
+/* Static description of a status code (never NULL). */
+const char* mo_status_string(int status);
+
+/* MO_ABI_VERSION of the loaded library. */
+int mo_abi_version(void);
+
+/* ---- host-side planning, exposed for inspection and testing (no CUDA) ---- */
+
+/* One output tile of a grouped Newton-Schulz GEMM launch. */
+typedef struct {
+  uint32_t mat;   /* index into the shape table */
+  uint16_t tm;    /* tile row (units of 128 rows) */
+  uint16_t tn;    /* tile column (units of 256 columns) */
+} mo_tile;
+
+enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
+
+/* Writes the tile schedule of one phase (in launch order) into out[0..cap)
+ * and the tile count into *count. Returns MO_OK, or MO_ERR_BAD_SHAPE if cap is
+ * too small (then *count holds the required size). Tiles are sorted by
+ * decreasing reduction length K (n for the Gram, m otherwise), ties broken by
+ * table index, then tile row, then tile column. Gram and A.A tiles cover only
+ * tiles that touch the upper triangle (col_end > row_begin). */
+int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase,
+                          mo_tile* out, int64_t cap, int64_t* count);
+
+/* ---- diagnostics ---- */
+
+/* Launches one CTA that waits on a barrier nothing will complete, with a
+ * bounded wait of `timeout_ns` nanoseconds (clamped to [1e3, 1e10]); on
+ * expiry it records MO_ERR_DEVICE_TIMEOUT in the device status word and
+ * returns. Used to test the bounded-wait error path without hanging. */
+int mo_selftest_bounded_wait(int64_t timeout_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MO_H_ */

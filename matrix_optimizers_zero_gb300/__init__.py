@@ -1,0 +1,278 @@
+"""GB300 (sm_103a) owner-local optimizer step: Muon on whole 2D matrices,
+AdamW on the packed tail, RMNP row normalisation.
+
+This module is a thin ctypes binding over the C ABI in include/mo.h: it only
+marshals torch tensors into the C tables and raises on error statuses. Every
+step of the computation runs in the library's CUDA kernels; there is no
+Python or CPU fallback, and importing the binding fails loudly when the
+library has not been built (python -m matrix_optimizers_zero_gb300.build).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, List, Optional, Sequence, Tuple
+
+from .build import LIB_PATH
+
+__all__ = [
+    "MoError", "MuonParams", "RmnpParams", "AdamWParams", "load_library",
+    "mo_muon_workspace_bytes", "muon_workspace", "muon_owner_step", "muon_owner_step_timed",
+    "rmnp_step", "rmnp_step_scaled", "adamw_tail_step", "mo_last_device_error",
+    "mo_status_string", "mo_selftest_bounded_wait", "mo_muon_tile_schedule", "MuonTable",
+    "TailTable", "RmnpTable",
+]
+
+MO_OK = 0
+PHASE_GRAM, PHASE_POLY, PHASE_UPDATE = 0, 1, 2
+
+
+class MoMatrix(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("G", ctypes.c_void_p), ("V", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+class MuonParams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("wd", ctypes.c_float), ("mu", ctypes.c_float),
+                ("a", ctypes.c_float), ("b", ctypes.c_float), ("c", ctypes.c_float),
+                ("eps", ctypes.c_float), ("ns_steps", ctypes.c_int32)]
+
+    def __init__(self, lr=0.02, wd=0.01, mu=0.95, a=3.4445, b=-4.7750, c=2.0315, eps=1e-7, ns_steps=5):
+        super().__init__(lr, wd, mu, a, b, c, eps, ns_steps)
+
+
+class RmnpParams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("wd", ctypes.c_float), ("mu", ctypes.c_float),
+                ("eps", ctypes.c_float)]
+
+    def __init__(self, lr=0.02, wd=0.01, mu=0.95, eps=1e-12):
+        super().__init__(lr, wd, mu, eps)
+
+
+class MoTailSeg(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_void_p), ("g", ctypes.c_void_p), ("m", ctypes.c_void_p),
+                ("v", ctypes.c_void_p), ("numel", ctypes.c_int64)]
+
+
+class AdamWParams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("wd", ctypes.c_float), ("beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("eps", ctypes.c_float), ("step", ctypes.c_int64)]
+
+    def __init__(self, lr=1e-3, wd=1e-2, beta1=0.9, beta2=0.95, eps=1e-8, step=1):
+        super().__init__(lr, wd, beta1, beta2, eps, step)
+
+
+class MoTile(ctypes.Structure):
+    _fields_ = [("mat", ctypes.c_uint32), ("tm", ctypes.c_uint16), ("tn", ctypes.c_uint16)]
+
+
+class MoError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = mo_status_string(status)
+        if status == -7:
+            msg += f" (cudaError {load_library().mo_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{status}]")
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Loads the in-tree libmo.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m matrix_optimizers_zero_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "mo_muon_workspace_bytes": (SZ, [P, I32, P]),
+        "muon_owner_step": (ctypes.c_int, [P, I32, P, P, SZ, P]),
+        "muon_owner_step_timed": (ctypes.c_int, [P, I32, P, P, SZ, P, P, P]),
+        "adamw_tail_step": (ctypes.c_int, [P, I32, P, P]),
+        "rmnp_step": (ctypes.c_int, [P, I32, P, P]),
+        "rmnp_step_scaled": (ctypes.c_int, [P, P, I32, P, P]),
+        "mo_last_device_error": (ctypes.c_int, [P]),
+        "mo_last_cuda_error": (ctypes.c_int, []),
+        "mo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "mo_abi_version": (ctypes.c_int, []),
+        "mo_muon_tile_schedule": (ctypes.c_int, [P, I32, I32, P, I64, P]),
+        "mo_selftest_bounded_wait": (ctypes.c_int, [I64, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != MO_OK:
+        raise MoError(status, where)
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def mo_status_string(status: int) -> str:
+    return load_library().mo_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- tables
+
+class MuonTable:
+    """ctypes shape table for a list of (W fp32, G bf16, V fp32) CUDA tensors.
+    Build it once and reuse it across steps to keep host overhead out of the
+    step."""
+
+    def __init__(self, mats: Sequence[Tuple["object", "object", "object"]]):
+        import torch
+        self.n = len(mats)
+        self.arr = (MoMatrix * max(1, self.n))()
+        for i, (W, G, V) in enumerate(mats):
+            if W.dtype != torch.float32 or V.dtype != torch.float32 or G.dtype != torch.bfloat16:
+                raise TypeError("expected W fp32, G bf16, V fp32")
+            if W.dim() != 2 or W.shape != G.shape or W.shape != V.shape:
+                raise ValueError("W, G, V must be 2D with equal shapes")
+            if not (W.is_contiguous() and G.is_contiguous() and V.is_contiguous()):
+                raise ValueError("W, G, V must be contiguous")
+            self.arr[i] = MoMatrix(W.data_ptr(), G.data_ptr(), V.data_ptr(), W.shape[0], W.shape[1])
+        self.keep = list(mats)
+
+    @property
+    def ptr(self):
+        return ctypes.cast(self.arr, ctypes.c_void_p) if self.n else None
+
+
+RmnpTable = MuonTable
+
+
+class TailTable:
+    """ctypes table of AdamW tail segments (p, g, m, v) fp32 CUDA tensors."""
+
+    def __init__(self, segs: Sequence[Tuple["object", "object", "object", "object"]]):
+        import torch
+        self.n = len(segs)
+        self.arr = (MoTailSeg * max(1, self.n))()
+        for i, (p, g, m, v) in enumerate(segs):
+            for t in (p, g, m, v):
+                if t.dtype != torch.float32 or not t.is_contiguous():
+                    raise TypeError("tail tensors must be contiguous fp32")
+                if t.numel() != p.numel():
+                    raise ValueError("p, g, m, v must have equal sizes")
+            self.arr[i] = MoTailSeg(p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr(), p.numel())
+        self.keep = list(segs)
+
+    @property
+    def ptr(self):
+        return ctypes.cast(self.arr, ctypes.c_void_p) if self.n else None
+
+
+def _as_table(mats, cls=MuonTable):
+    return mats if isinstance(mats, cls) else cls(mats)
+
+
+# ---------------------------------------------------------------- Muon
+
+def mo_muon_workspace_bytes(mats, params: Optional[MuonParams] = None) -> int:
+    t = _as_table(mats)
+    params = params or MuonParams()
+    return int(load_library().mo_muon_workspace_bytes(t.ptr, t.n, ctypes.byref(params)))
+
+
+def muon_workspace(mats, params: Optional[MuonParams] = None, device=None):
+    """A torch uint8 device tensor large enough for muon_owner_step."""
+    import torch
+    t = _as_table(mats)
+    nbytes = mo_muon_workspace_bytes(t, params)
+    if device is None:
+        device = t.keep[0][0].device if t.n else torch.device("cuda")
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def muon_owner_step(mats, params: Optional[MuonParams] = None, workspace=None, stream=None) -> None:
+    t = _as_table(mats)
+    params = params or MuonParams()
+    if workspace is None:
+        raise ValueError("muon_owner_step needs a workspace (see muon_workspace())")
+    st = load_library().muon_owner_step(t.ptr, t.n, ctypes.byref(params), workspace.data_ptr(),
+                                        workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(st, "muon_owner_step")
+
+
+def muon_owner_step_timed(mats, params, workspace, ev_begin, ev_end, stream=None) -> None:
+    t = _as_table(mats)
+    st = load_library().muon_owner_step_timed(
+        t.ptr, t.n, ctypes.byref(params), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream), ev_begin.cuda_event if ev_begin is not None else None,
+        ev_end.cuda_event if ev_end is not None else None)
+    _check(st, "muon_owner_step_timed")
+
+
+# ---------------------------------------------------------------- RMNP / AdamW
+
+def rmnp_step(mats, params: Optional[RmnpParams] = None, stream=None) -> None:
+    t = _as_table(mats)
+    params = params or RmnpParams()
+    _check(load_library().rmnp_step(t.ptr, t.n, ctypes.byref(params), _stream_ptr(stream)), "rmnp_step")
+
+
+def rmnp_step_scaled(mats, scales: Sequence[float], params: Optional[RmnpParams] = None, stream=None) -> None:
+    t = _as_table(mats)
+    params = params or RmnpParams()
+    arr = (ctypes.c_float * max(1, len(scales)))(*[float(s) for s in scales])
+    _check(load_library().rmnp_step_scaled(t.ptr, ctypes.cast(arr, ctypes.c_void_p), t.n,
+                                           ctypes.byref(params), _stream_ptr(stream)), "rmnp_step_scaled")
+
+
+def adamw_tail_step(segs, params: Optional[AdamWParams] = None, stream=None) -> None:
+    t = segs if isinstance(segs, TailTable) else TailTable(segs)
+    params = params or AdamWParams()
+    _check(load_library().adamw_tail_step(t.ptr, t.n, ctypes.byref(params), _stream_ptr(stream)),
+           "adamw_tail_step")
+
+
+# ---------------------------------------------------------------- diagnostics
+
+def mo_last_device_error(stream=None) -> int:
+    return int(load_library().mo_last_device_error(_stream_ptr(stream)))
+
+
+def mo_selftest_bounded_wait(timeout_ns: int, stream=None) -> None:
+    _check(load_library().mo_selftest_bounded_wait(int(timeout_ns), _stream_ptr(stream)), "selftest")
+
+
+def fake_table(shapes: Sequence[Tuple[int, int]]):
+    """A MoMatrix array with distinct, aligned, non-overlapping fake addresses
+    (never dereferenced) for the host-only planning entry points."""
+    arr = (MoMatrix * max(1, len(shapes)))()
+    addr = 1 << 20
+    for i, (r, c) in enumerate(shapes):
+        sz = ((r * c * 4 + 4095) // 4096) * 4096
+        w, g, v = addr, addr + sz, addr + 2 * sz
+        addr += 3 * sz
+        arr[i] = MoMatrix(w, g, v, r, c)
+    return arr
+
+
+def mo_muon_tile_schedule(shapes: Sequence[Tuple[int, int]], phase: int) -> List[Tuple[int, int, int]]:
+    lib = load_library()
+    arr = fake_table(shapes)
+    count = ctypes.c_int64(0)
+    st = lib.mo_muon_tile_schedule(ctypes.cast(arr, ctypes.c_void_p), len(shapes), phase, None, 0,
+                                   ctypes.byref(count))
+    if st not in (MO_OK, -2):
+        _check(st, "mo_muon_tile_schedule")
+    out = (MoTile * max(1, count.value))()
+    _check(lib.mo_muon_tile_schedule(ctypes.cast(arr, ctypes.c_void_p), len(shapes), phase,
+                                     ctypes.cast(out, ctypes.c_void_p), count.value, ctypes.byref(count)),
+           "mo_muon_tile_schedule")
+    return [(t.mat, t.tm, t.tn) for t in out[:count.value]]

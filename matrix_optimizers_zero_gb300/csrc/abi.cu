@@ -1,0 +1,330 @@
+// extern "C" entry points of include/mo.h: validation, planning, workspace
+// binding and kernel launches. No entry point allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <array>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kernels.h"
+#include "mo.h"
+#include "mo_internal.h"
+#include "plan.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = int(e);
+  return MO_ERR_CUDA;
+}
+
+// Per-device facts looked up once: compute capability, SM count, the
+// device-side status word.
+struct DeviceInfo {
+  int checked = 0;
+  int supported = 0;
+  int sms = 0;
+  int* status = nullptr;
+};
+std::array<DeviceInfo, 64> g_dev;
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= int(g_dev.size())) return MO_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[size_t(dev)];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    int* st = nullptr;
+    if ((e = mo::device_status_ptr(&st)) != cudaSuccess) return cuda_fail(e);
+    d.supported = (major == 10 && minor == 3) ? 1 : 0;
+    d.sms = sms;
+    d.status = st;
+    d.checked = 1;
+  }
+  if (!d.supported) return MO_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return MO_OK;
+}
+
+int muon_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* ws, size_t ws_bytes,
+              cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
+  int st = mo::validate_muon_params(prm);
+  if (st != MO_OK) return st;
+  if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
+  if (n == 0) {
+    cudaError_t e;
+    if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) return cuda_fail(e);
+    if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return cuda_fail(e);
+    return MO_OK;
+  }
+  if (!ws) return MO_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MO_ERR_MISALIGNED;
+  mo::MuonLayout L;
+  mo::plan_muon(tbl, n, L);
+  if (ws_bytes < L.total_bytes) return MO_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MO_OK) return st;
+
+  // bind workspace offsets to addresses and build the header image
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  std::vector<uint8_t> header(L.header_bytes, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    mo::DevMat& d = L.mats[size_t(i)];
+    d.X[0] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[0]));
+    d.X[1] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[1]));
+    d.A = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.A));
+    d.B = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.B));
+    if (!mo::encode_matrix_maps(d, header.data() + L.off_tmaps + size_t(i) * mo::kMapsPerMat * mo::kTensorMapBytes))
+      return cuda_fail(cudaErrorInvalidValue);
+  }
+  std::memcpy(header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * size_t(n));
+  std::memcpy(header.data() + L.off_nrm_prefix, L.nrm_prefix.data(), sizeof(int64_t) * (size_t(n) + 1));
+  std::memcpy(header.data() + L.off_cast_prefix, L.cast_prefix.data(), sizeof(int64_t) * (size_t(n) + 1));
+  for (int ph = 0; ph < 3; ++ph)
+    if (!L.tiles[ph].empty())
+      std::memcpy(header.data() + L.off_tiles[ph], L.tiles[ph].data(), sizeof(mo::TileRec) * L.tiles[ph].size());
+
+  cudaError_t e = cudaMemcpyAsync(ws, header.data(), L.header_bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  const mo::DevMat* d_mats = reinterpret_cast<const mo::DevMat*>(wsb + L.off_meta);
+  float* d_scales = reinterpret_cast<float*>(wsb + L.off_scales);
+
+  mo::ProParams pp{};
+  pp.mats = d_mats;
+  pp.nrm_prefix = reinterpret_cast<const int64_t*>(wsb + L.off_nrm_prefix);
+  pp.cast_prefix = reinterpret_cast<const int64_t*>(wsb + L.off_cast_prefix);
+  pp.partials = reinterpret_cast<float*>(wsb + L.off_partials);
+  pp.counters = reinterpret_cast<uint32_t*>(wsb + L.off_counters);
+  pp.scales = d_scales;
+  pp.n = n;
+  pp.nrm_total = L.nrm_total;
+  pp.cast_total = L.cast_total;
+  pp.mu = prm->mu;
+  pp.eps = prm->eps;
+  const int64_t ew_grid = int64_t(dev->sms) * 8;
+  if ((e = mo::launch_muon_momentum_norm(pp, int(std::min<int64_t>(L.nrm_total, ew_grid)), stream)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = mo::launch_muon_normalize_cast(pp, int(std::min<int64_t>(L.cast_total, ew_grid)), stream)) != cudaSuccess)
+    return cuda_fail(e);
+  if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) return cuda_fail(e);
+
+  mo::NsParams np{};
+  np.mats = d_mats;
+  np.tmaps = reinterpret_cast<const CUtensorMap*>(wsb + L.off_tmaps);
+  np.status = dev->status;
+  np.a = prm->a;
+  np.b = prm->b;
+  np.c = prm->c;
+  np.lr = prm->lr;
+  np.decay = float(1.0 - double(prm->lr) * double(prm->wd));
+  np.timeout_ns = 2000000000ull;
+  int cur = 0;
+  for (int it = 0; it < prm->ns_steps; ++it) {
+    np.cur = cur;
+    for (int ph = 0; ph < 3; ++ph) {
+      np.tiles = reinterpret_cast<const mo::TileRec*>(wsb + L.off_tiles[ph]);
+      np.ntiles = int32_t(L.tiles[ph].size());
+      const int grid = std::max(1, std::min(np.ntiles, dev->sms));
+      const bool last = (ph == MO_PHASE_UPDATE) && (it == prm->ns_steps - 1);
+      if ((e = mo::launch_ns_phase(ph, last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
+    }
+    cur ^= 1;
+  }
+  if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return cuda_fail(e);
+  return MO_OK;
+}
+
+int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmnp_params* prm,
+              cudaStream_t stream) {
+  int st = mo::validate_rmnp_params(prm);
+  if (st != MO_OK) return st;
+  if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
+  if (scales)
+    for (int32_t i = 0; i < n; ++i)
+      if (!std::isfinite(scales[i])) return MO_ERR_BAD_PARAM;
+  if (n == 0) return MO_OK;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MO_OK) return st;
+  static thread_local mo::RmnpParams rp;   // ~25 KB: keep off the stack
+  for (int32_t b = 0; b < n; b += mo::kRmnpMaxEntries) {
+    const int32_t cnt = std::min<int32_t>(mo::kRmnpMaxEntries, n - b);
+    std::memset(&rp, 0, sizeof(rp));
+    rp.n = cnt;
+    rp.decay = float(1.0 - double(prm->lr) * double(prm->wd));
+    rp.lr = prm->lr;
+    rp.mu = prm->mu;
+    rp.eps = prm->eps;
+    int64_t rows = 0;
+    for (int32_t i = 0; i < cnt; ++i) {
+      const mo_matrix& t = tbl[b + i];
+      mo::RmnpEntry& E = rp.e[i];
+      E.W = t.W;
+      E.G = static_cast<const uint16_t*>(t.G);
+      E.V = t.V;
+      E.R = int32_t(t.rows);
+      E.C = int32_t(t.cols);
+      E.scale = scales ? scales[b + i] : float(std::sqrt(std::max(1.0, double(t.rows) / double(t.cols))));
+      E.vec_ok = (t.cols % 4 == 0) ? 1 : 0;
+      rp.row_prefix[i] = rows;
+      rows += t.rows;
+    }
+    rp.row_prefix[cnt] = rows;
+    const int64_t warps_needed = rows;
+    const int grid = int(std::max<int64_t>(1, std::min<int64_t>((warps_needed + 7) / 8, int64_t(dev->sms) * 8)));
+    cudaError_t e = mo::launch_rmnp(rp, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return MO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_params* params) {
+  if (mo::validate_muon_params(params) != MO_OK) return 0;
+  if (mo::validate_matrix_table(tbl, n) != MO_OK) return 0;
+  if (n == 0) return 0;
+  mo::MuonLayout L;
+  mo::plan_muon(tbl, n, L);
+  return L.total_bytes;
+}
+
+int muon_owner_step(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+  return muon_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws,
+                          size_t ws_bytes, cudaStream_t stream, cudaEvent_t ev_ns_begin, cudaEvent_t ev_ns_end) {
+  return muon_impl(tbl, n, params, ws, ws_bytes, stream, ev_ns_begin, ev_ns_end);
+}
+
+int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cudaStream_t stream) {
+  return rmnp_impl(tbl, nullptr, n, params, stream);
+}
+
+int rmnp_step_scaled(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmnp_params* params,
+                     cudaStream_t stream) {
+  if (n > 0 && !scales) return MO_ERR_NULL_POINTER;
+  return rmnp_impl(tbl, scales, n, params, stream);
+}
+
+int adamw_tail_step(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* params, cudaStream_t stream) {
+  int st = mo::validate_adamw(segs, n, params);
+  if (st != MO_OK) return st;
+  if (n == 0) return MO_OK;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MO_OK) return st;
+  const double t = double(params->step);
+  const double bc1 = 1.0 - std::pow(double(params->beta1), t);
+  const double bc2 = 1.0 - std::pow(double(params->beta2), t);
+  static thread_local mo::AdamParams ap;
+  int32_t i = 0;
+  while (i < n) {
+    std::memset(&ap, 0, sizeof(ap));
+    ap.decay = float(1.0 - double(params->lr) * double(params->wd));
+    ap.step_size = float(double(params->lr) / bc1);
+    ap.inv_bc2_sqrt = float(1.0 / std::sqrt(bc2));
+    ap.beta1 = params->beta1;
+    ap.beta2 = params->beta2;
+    ap.eps = params->eps;
+    int32_t cnt = 0;
+    int64_t items = 0;
+    for (; i < n && cnt < mo::kAdamMaxSegs; ++i) {
+      const mo_tail_seg& s = segs[i];
+      if (s.numel == 0) continue;
+      ap.s[cnt] = mo::AdamSeg{s.p, s.g, s.m, s.v, s.numel};
+      ap.item_prefix[cnt] = items;
+      items += (s.numel + mo::kAdamItem - 1) / mo::kAdamItem;
+      ++cnt;
+    }
+    ap.item_prefix[cnt] = items;
+    ap.n = cnt;
+    if (cnt == 0) break;
+    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items, int64_t(dev->sms) * 8)));
+    cudaError_t e = mo::launch_adamw(ap, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return MO_OK;
+}
+
+int mo_last_device_error(cudaStream_t stream) {
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != MO_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int val = 0;
+  if ((e = cudaMemcpy(&val, dev->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+  if (val != 0) {
+    const int zero = 0;
+    if ((e = cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  return val;
+}
+
+int mo_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* mo_status_string(int status) {
+  switch (status) {
+    case MO_OK: return "ok";
+    case MO_ERR_NULL_POINTER: return "null pointer";
+    case MO_ERR_BAD_SHAPE: return "bad shape or size";
+    case MO_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case MO_ERR_BAD_PARAM: return "hyperparameter NaN/Inf or out of range";
+    case MO_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MO_ERR_OVERLAP: return "written buffers overlap";
+    case MO_ERR_CUDA: return "CUDA runtime error";
+    case MO_ERR_DEVICE_TIMEOUT: return "bounded device-side wait expired";
+    case MO_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+int mo_abi_version(void) { return MO_ABI_VERSION; }
+
+int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase, mo_tile* out, int64_t cap,
+                          int64_t* count) {
+  if (!count) return MO_ERR_NULL_POINTER;
+  if (phase < 0 || phase > 2) return MO_ERR_BAD_PARAM;
+  int st = mo::validate_matrix_table(tbl, n);
+  if (st != MO_OK) return st;
+  std::vector<mo::TileRec> tiles;
+  mo::build_tiles(tbl, n, phase, tiles);
+  *count = int64_t(tiles.size());
+  if (cap < int64_t(tiles.size())) return MO_ERR_BAD_SHAPE;
+  if (!tiles.empty()) {
+    if (!out) return MO_ERR_NULL_POINTER;
+    std::memcpy(out, tiles.data(), tiles.size() * sizeof(mo_tile));
+  }
+  return MO_OK;
+}
+
+int mo_selftest_bounded_wait(int64_t timeout_ns, cudaStream_t stream) {
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != MO_OK) return st;
+  const int64_t t = std::min<int64_t>(std::max<int64_t>(timeout_ns, 1000), 10000000000ll);
+  cudaError_t e = mo::launch_bounded_wait_selftest(dev->status, uint64_t(t), stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MO_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,373 @@
+// Memory-bound kernels of the owner-local step: the fused Muon prologue
+// (momentum + Frobenius sum of squares + bf16 cast/transpose), RMNP and
+// AdamW. All accesses along rows are 16-byte vectors where the row length
+// allows it; every kernel is a grid-stride loop over a flat work list sized to
+// a multiple of the SM count.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "kernels.h"
+#include "mo_internal.h"
+
+namespace mo {
+
+namespace {
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+
+// ------------------------------------------------------------------ Muon prologue
+//
+// Pass 1: momentum V <- mu V + G ("Optimizers In A Sharded World", section 1)
+// over flat 8192-element chunks of each stored matrix, with one fp32 sum of
+// squares per chunk. The CTA that completes a matrix's last chunk sums that
+// matrix's partials in a fixed order (deterministic, no float atomics) and
+// writes the Frobenius scale 1 / (||V|| + eps) (the appendix of the same page:
+// eps is added to the norm).
+__global__ void __launch_bounds__(256) muon_momentum_norm_kernel(const __grid_constant__ ProParams p) {
+  __shared__ float red[8];
+  __shared__ int last_flag;
+  const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
+  for (int64_t t = blockIdx.x; t < p.nrm_total; t += gridDim.x) {
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.nrm_prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int mi = lo;
+    const DevMat& M = p.mats[mi];
+    const int64_t total = int64_t(M.R) * int64_t(M.C);
+    const int64_t e0 = (t - p.nrm_prefix[mi]) * kNrmChunk;
+    float* __restrict__ V = M.V;
+    const uint16_t* __restrict__ G = M.G;
+    float4 v[8];
+    uint2 g[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t e = e0 + int64_t(j * 256 + tid) * 4;
+      if (e + 4 <= total) {
+        v[j] = *reinterpret_cast<const float4*>(V + e);
+        g[j] = *reinterpret_cast<const uint2*>(G + e);
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int64_t e = e0 + int64_t(j * 256 + tid) * 4;
+      if (e + 4 <= total) {
+        float4 n4;
+        n4.x = fmaf(p.mu, v[j].x, bf16_bits_to_float(g[j].x & 0xFFFFu));
+        n4.y = fmaf(p.mu, v[j].y, bf16_bits_to_float(g[j].x >> 16));
+        n4.z = fmaf(p.mu, v[j].z, bf16_bits_to_float(g[j].y & 0xFFFFu));
+        n4.w = fmaf(p.mu, v[j].w, bf16_bits_to_float(g[j].y >> 16));
+        *reinterpret_cast<float4*>(V + e) = n4;
+        ss = fmaf(n4.x, n4.x, ss);
+        ss = fmaf(n4.y, n4.y, ss);
+        ss = fmaf(n4.z, n4.z, ss);
+        ss = fmaf(n4.w, n4.w, ss);
+      } else {
+        for (int64_t k = e; k < total && k < e + 4; ++k) {
+          const float vn = fmaf(p.mu, V[k], bf16_bits_to_float(G[k]));
+          V[k] = vn;
+          ss = fmaf(vn, vn, ss);
+        }
+      }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) tot += red[w];
+      p.partials[t] = tot;
+      __threadfence();
+      const uint32_t prev = atomicAdd(&p.counters[mi], 1u);
+      last_flag = (int64_t(prev) + 1 == M.nrm_count) ? 1 : 0;
+    }
+    __syncthreads();
+    if (last_flag) {
+      __threadfence();
+      float acc = 0.f;
+      for (int64_t k = tid; k < M.nrm_count; k += 256) acc += __ldcg(p.partials + M.nrm_base + k);
+      acc = warp_sum(acc);
+      if (lane == 0) red[warp] = acc;
+      __syncthreads();
+      if (tid == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) tot += red[w];
+        p.scales[mi] = 1.0f / (sqrtf(tot) + p.eps);
+        p.counters[mi] = 0u;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Pass 2: X0 = bf16(V * scale), written in the wide orientation: X = V for
+// rows <= cols, X = V^T (through a shared-memory transpose) otherwise
+// (appendix of "Optimizers In A Sharded World": transpose when rows > cols).
+// 64 x 128 tiles of the stored matrix; X rows are padded to ldx.
+__global__ void __launch_bounds__(256) muon_normalize_cast_kernel(const __grid_constant__ ProParams p) {
+  __shared__ __align__(16) uint16_t tbuf[kCastTC][kCastTR + 8];
+  const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
+  for (int64_t t = blockIdx.x; t < p.cast_total; t += gridDim.x) {
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.cast_prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int mi = lo;
+    const DevMat& M = p.mats[mi];
+    const int64_t local = t - p.cast_prefix[mi];
+    const int r0 = int(local / M.cast_tiles_c) * kCastTR;
+    const int c0 = int(local % M.cast_tiles_c) * kCastTC;
+    const int R = M.R, C = M.C;
+    const int cl = lane * 4;
+    const int c = c0 + cl;
+    const bool tall = M.tall != 0;
+    const float sc = p.scales[mi];
+    uint16_t* X = M.X[0];
+    const size_t ldx = size_t(M.ldx);
+#pragma unroll 4
+    for (int i = 0; i < kCastTR / 8; ++i) {
+      const int rl = warp + 8 * i;
+      const int r = r0 + rl;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (r < R && c < C) {
+        const size_t off = size_t(r) * size_t(C) + size_t(c);
+        if (M.vec_ok && c + 4 <= C) {
+          const float4 v4 = *reinterpret_cast<const float4*>(M.V + off);
+          x[0] = v4.x * sc;
+          x[1] = v4.y * sc;
+          x[2] = v4.z * sc;
+          x[3] = v4.w * sc;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (c + q < C) x[q] = M.V[off + q] * sc;
+        }
+      }
+      if (!tall) {
+        if (r < R && c < C) {
+          uint16_t* xp = X + size_t(r) * ldx + size_t(c);
+          if (c + 4 <= C) {
+            *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (c + q < C) xp[q] = float_to_bf16_bits(x[q]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tbuf[cl + q][rl] = float_to_bf16_bits(x[q]);
+      }
+    }
+    if (tall) {
+      __syncthreads();
+      // X is [C, R]: X[c][r] = bf16(V[r][c] * scale); 16-byte segments of 8 rows
+      for (int k = tid; k < kCastTC * (kCastTR / 8); k += 256) {
+        const int cc = k >> 3, seg = k & 7;
+        const int xc = c0 + cc;
+        const int xr = r0 + seg * 8;
+        if (xc < C && xr < R) {
+          uint16_t* xp = X + size_t(xc) * ldx + size_t(xr);
+          const uint16_t* sp = &tbuf[cc][seg * 8];
+          if (xr + 8 <= R) {
+            *reinterpret_cast<uint4*>(xp) = *reinterpret_cast<const uint4*>(sp);
+          } else {
+            for (int j = 0; j < 8; ++j)
+              if (xr + j < R) xp[j] = sp[j];
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// ------------------------------------------------------------------ RMNP
+//
+// One warp per stored row ("Optimizers In A Sharded World", section 1 and the
+// appendix rmnp_local): V_i <- mu V_i + G_i, D_i = V_i / max(||V_i||_2, eps),
+// W_i <- W_i (1 - lr wd) - lr s D_i. Pass 1 writes V_i and accumulates its sum
+// of squares in fp32 (lane-strided, then a fixed xor-shuffle tree, so a row's
+// result does not depend on which other rows share the launch); pass 2 re-reads
+// V_i (just written, served from L2) and updates W_i.
+__global__ void __launch_bounds__(256) rmnp_kernel(const __grid_constant__ RmnpParams p) {
+  const int lane = int(threadIdx.x & 31);
+  const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t total = p.row_prefix[p.n];
+  for (int64_t row = gw; row < total; row += nw) {
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.row_prefix[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const RmnpEntry& E = p.e[lo];
+    const int C = E.C;
+    const size_t off = size_t(row - p.row_prefix[lo]) * size_t(C);
+    float* __restrict__ Vr = E.V + off;
+    float* __restrict__ Wr = E.W + off;
+    const uint16_t* __restrict__ Gr = E.G + off;
+    float ss = 0.f;
+    if (E.vec_ok) {
+      for (int cb = lane * 4; cb < C; cb += 4 * 128) {
+        float4 v[4];
+        uint2 g[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 128;
+          if (cc < C) {
+            v[u] = *reinterpret_cast<const float4*>(Vr + cc);
+            g[u] = *reinterpret_cast<const uint2*>(Gr + cc);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 128;
+          if (cc < C) {
+            float4 n4;
+            n4.x = fmaf(p.mu, v[u].x, bf16_bits_to_float(g[u].x & 0xFFFFu));
+            n4.y = fmaf(p.mu, v[u].y, bf16_bits_to_float(g[u].x >> 16));
+            n4.z = fmaf(p.mu, v[u].z, bf16_bits_to_float(g[u].y & 0xFFFFu));
+            n4.w = fmaf(p.mu, v[u].w, bf16_bits_to_float(g[u].y >> 16));
+            *reinterpret_cast<float4*>(Vr + cc) = n4;
+            ss = fmaf(n4.x, n4.x, ss);
+            ss = fmaf(n4.y, n4.y, ss);
+            ss = fmaf(n4.z, n4.z, ss);
+            ss = fmaf(n4.w, n4.w, ss);
+          }
+        }
+      }
+    } else {
+      for (int cc = lane; cc < C; cc += 32) {
+        const float vn = fmaf(p.mu, Vr[cc], bf16_bits_to_float(Gr[cc]));
+        Vr[cc] = vn;
+        ss = fmaf(vn, vn, ss);
+      }
+    }
+    ss = warp_sum(ss);
+    const float k = p.lr * E.scale / fmaxf(sqrtf(ss), p.eps);
+    if (E.vec_ok) {
+      for (int cb = lane * 4; cb < C; cb += 4 * 128) {
+        float4 v[4], w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 128;
+          if (cc < C) {
+            v[u] = *reinterpret_cast<const float4*>(Vr + cc);
+            w[u] = *reinterpret_cast<const float4*>(Wr + cc);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 128;
+          if (cc < C) {
+            float4 o;
+            o.x = w[u].x * p.decay - k * v[u].x;
+            o.y = w[u].y * p.decay - k * v[u].y;
+            o.z = w[u].z * p.decay - k * v[u].z;
+            o.w = w[u].w * p.decay - k * v[u].w;
+            *reinterpret_cast<float4*>(Wr + cc) = o;
+          }
+        }
+      }
+    } else {
+      for (int cc = lane; cc < C; cc += 32) Wr[cc] = Wr[cc] * p.decay - k * Vr[cc];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ AdamW
+//
+// Decoupled AdamW with bias correction on the packed tail ("MatrixFSDP",
+// sections 3 and 5.1). Work items of 4096 elements; each thread handles four
+// 16-byte vectors per item, loads issued before use.
+__device__ __forceinline__ void adam_elem(const AdamParams& p, float& pp, float g, float& m, float& v) {
+  m = fmaf(p.beta1, m, (1.0f - p.beta1) * g);
+  v = fmaf(p.beta2, v, (1.0f - p.beta2) * g * g);
+  const float denom = fmaf(sqrtf(v), p.inv_bc2_sqrt, p.eps);
+  pp = pp * p.decay - p.step_size * (m / denom);
+}
+
+__global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamParams p) {
+  const int64_t total = p.item_prefix[p.n];
+  for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.item_prefix[mid] <= it) lo = mid; else hi = mid - 1;
+    }
+    const AdamSeg& S = p.s[lo];
+    const int64_t e0 = (it - p.item_prefix[lo]) * kAdamItem;
+    float4 P[4], G[4], Mm[4], Vv[4];
+    bool full[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t e = e0 + int64_t(u * 256 + int(threadIdx.x)) * 4;
+      full[u] = e + 4 <= S.numel;
+      if (full[u]) {
+        P[u] = *reinterpret_cast<const float4*>(S.p + e);
+        G[u] = *reinterpret_cast<const float4*>(S.g + e);
+        Mm[u] = *reinterpret_cast<const float4*>(S.m + e);
+        Vv[u] = *reinterpret_cast<const float4*>(S.v + e);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t e = e0 + int64_t(u * 256 + int(threadIdx.x)) * 4;
+      if (full[u]) {
+        adam_elem(p, P[u].x, G[u].x, Mm[u].x, Vv[u].x);
+        adam_elem(p, P[u].y, G[u].y, Mm[u].y, Vv[u].y);
+        adam_elem(p, P[u].z, G[u].z, Mm[u].z, Vv[u].z);
+        adam_elem(p, P[u].w, G[u].w, Mm[u].w, Vv[u].w);
+        *reinterpret_cast<float4*>(S.p + e) = P[u];
+        *reinterpret_cast<float4*>(S.m + e) = Mm[u];
+        *reinterpret_cast<float4*>(S.v + e) = Vv[u];
+      } else if (e < S.numel) {
+        for (int64_t j = e; j < S.numel && j < e + 4; ++j) {
+          float pp = S.p[j], mm = S.m[j], vv = S.v[j];
+          adam_elem(p, pp, S.g[j], mm, vv);
+          S.p[j] = pp;
+          S.m[j] = mm;
+          S.v[j] = vv;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_muon_momentum_norm(const ProParams& p, int grid, cudaStream_t stream) {
+  if (p.nrm_total <= 0) return cudaSuccess;
+  muon_momentum_norm_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_muon_normalize_cast(const ProParams& p, int grid, cudaStream_t stream) {
+  if (p.cast_total <= 0) return cudaSuccess;
+  muon_normalize_cast_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmnp(const RmnpParams& p, int grid, cudaStream_t stream) {
+  if (p.n <= 0 || p.row_prefix[p.n] <= 0) return cudaSuccess;
+  rmnp_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(const AdamParams& p, int grid, cudaStream_t stream) {
+  if (p.n <= 0 || p.item_prefix[p.n] <= 0) return cudaSuccess;
+  adamw_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mo

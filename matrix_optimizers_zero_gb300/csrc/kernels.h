@@ -1,0 +1,88 @@
+// Launch interface between the C-ABI layer (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mo_internal.h"
+
+namespace mo {
+
+// ---------------------------------------------------------------- NS GEMMs
+struct NsParams {
+  const DevMat* mats;
+  const CUtensorMap* tmaps;   // kMapsPerMat per matrix: X[0], X[1], A, B
+  const TileRec* tiles;
+  int* status;                // device status word
+  int32_t ntiles;
+  int32_t cur;                // X buffer read by this launch
+  float a, b, c;
+  float lr;
+  float decay;                // 1 - lr wd, rounded once from double on the host
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream);
+size_t ns_gemm_smem_bytes();
+bool encode_matrix_maps(const DevMat& d, void* out_maps);   // writes kMapsPerMat CUtensorMap
+cudaError_t device_status_ptr(int** out);
+cudaError_t launch_bounded_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream);
+
+// ---------------------------------------------------------------- Muon prologue
+struct ProParams {
+  const DevMat* mats;
+  const int64_t* nrm_prefix;  // n + 1 prefix sums of sum-of-squares chunks
+  const int64_t* cast_prefix; // n + 1 prefix sums of normalise/cast tiles
+  float* partials;            // one sum of squares per chunk
+  uint32_t* counters;         // per matrix, zero on entry, zero again on exit
+  float* scales;              // out of pass 1: 1 / (||V_new||_F + eps)
+  int32_t n;
+  int64_t nrm_total;
+  int64_t cast_total;
+  float mu, eps;
+};
+cudaError_t launch_muon_momentum_norm(const ProParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_muon_normalize_cast(const ProParams& p, int grid, cudaStream_t stream);
+
+// ---------------------------------------------------------------- RMNP
+constexpr int kRmnpMaxEntries = 512;
+struct RmnpEntry {
+  float* W;
+  const uint16_t* G;
+  float* V;
+  int32_t R, C;
+  float scale;
+  int32_t vec_ok;
+};
+struct RmnpParams {
+  RmnpEntry e[kRmnpMaxEntries];
+  int64_t row_prefix[kRmnpMaxEntries + 1];
+  int32_t n;
+  float decay, lr, mu, eps;
+};
+cudaError_t launch_rmnp(const RmnpParams& p, int grid, cudaStream_t stream);
+
+// ---------------------------------------------------------------- AdamW
+constexpr int kAdamMaxSegs = 256;
+constexpr int kAdamItem = 4096;   // elements per work item (1024 float4)
+struct AdamSeg {
+  float* p;
+  const float* g;
+  float* m;
+  float* v;
+  int64_t numel;
+};
+struct AdamParams {
+  AdamSeg s[kAdamMaxSegs];
+  int64_t item_prefix[kAdamMaxSegs + 1];
+  int32_t n;
+  float decay;        // 1 - lr wd
+  float step_size;    // lr / (1 - beta1^t)
+  float inv_bc2_sqrt; // 1 / sqrt(1 - beta2^t)
+  float beta1, beta2, eps;
+};
+cudaError_t launch_adamw(const AdamParams& p, int grid, cudaStream_t stream);
+
+}  // namespace mo

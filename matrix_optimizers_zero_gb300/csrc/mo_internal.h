@@ -1,0 +1,62 @@
+// Internal layout shared by the host planner and the CUDA kernels.
+// Nothing here is part of the public ABI (include/mo.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "mo.h"
+
+namespace mo {
+
+// Newton-Schulz GEMM tiling: one UMMA M=128 x N=256 accumulator per tile,
+// 64-element (128-byte, one swizzle row) K blocks.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+
+// Muon prologue, pass 1 (momentum + sum of squares): flat chunks of the
+// row-major stored matrix. Pass 2 (normalise + bf16 cast, transposed for tall
+// matrices): 64 x 128 tiles of the stored matrix.
+constexpr int64_t kNrmChunk = 8192;
+constexpr int kCastTR = 64;
+constexpr int kCastTC = 128;
+
+// Supported maximum sizes (the A and B buffers are m x m).
+constexpr int64_t kMaxDim = int64_t(1) << 22;   // rows or cols
+constexpr int64_t kMaxM = 65536;                 // min(rows, cols)
+
+// Number of CUtensorMap objects per matrix: X ping, X pong, A, B.
+constexpr int kMapsPerMat = 4;
+constexpr size_t kTensorMapBytes = 128;
+
+// Device-side description of one matrix of the table.
+struct DevMat {
+  float* W;                 // [R, C] fp32
+  const uint16_t* G;        // [R, C] bf16
+  float* V;                 // [R, C] fp32
+  uint16_t* X[2];           // [m, ldx] bf16 ping-pong Newton-Schulz iterates
+  uint16_t* A;              // [m, lda] bf16 Gram
+  uint16_t* B;              // [m, lda] bf16 b A + c A A
+  int32_t R, C;             // stored shape
+  int32_t m, n;             // iteration shape (m <= n)
+  int32_t ldx, lda;         // row strides in elements (multiples of 64)
+  int32_t tall;             // R > C: X = V^T
+  int32_t vec_ok;           // C % 4 == 0 (16-byte vector access along rows)
+  int32_t cast_tiles_c;     // normalise/cast tiles along C
+  float shape_scale;        // sqrt(max(1, R/C))
+  int32_t pad0;
+  int64_t nrm_base;         // first sum-of-squares chunk (global index)
+  int64_t nrm_count;        // sum-of-squares chunks of this matrix
+};
+
+// Identical layout to mo_tile.
+struct TileRec {
+  uint32_t mat;
+  uint16_t tm;
+  uint16_t tn;
+};
+static_assert(sizeof(TileRec) == 8, "TileRec layout");
+static_assert(sizeof(mo_tile) == 8, "mo_tile layout");
+
+}  // namespace mo

@@ -1,0 +1,468 @@
+// Grouped Newton-Schulz GEMMs on the 5th-generation tensor cores (sm_103a).
+//
+// One launch computes one of the three products of a quintic iteration for
+// every matrix of the owner's table ("Optimizers In A Sharded World", section
+// 1 and appendix: five iterations of three products; the coefficients
+// (a, b, c) and the wide orientation m <= n):
+//   GRAM    A  = X X^T              (upper-triangle tiles, mirrored store)
+//   POLY    B  = b A + c (A A)      (upper-triangle tiles, mirrored store)
+//   UPDATE  X' = a X + B X          (all tiles; the last iteration applies
+//                                    W <- W (1 - lr wd) - lr s X' instead)
+// X0 = bf16(V / (||V||_F + eps)) is written by the prologue.
+//
+// Kernel structure (one persistent CTA per SM, 6 warps):
+//   warp 0      TMA producer: 128x64 A-operand and 256x64 B-operand boxes
+//               (128-byte swizzle) into a 4-stage shared-memory ring
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//               (M=128, N=256, K=16 per instruction, fp32 accumulate)
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane per
+//               thread), fused arithmetic, bf16/fp32 stores
+// The two 256-column accumulators in TMEM let the epilogue of one tile run
+// under the main loop of the next.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "device_common.cuh"
+#include "kernels.h"
+#include "mo_internal.h"
+#include "ptx.cuh"
+
+namespace mo {
+
+__device__ int g_mo_status = 0;
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;                 // one TMA box: 64 x 64 bf16
+constexpr uint32_t kTileABytes = kBM * kBK * 2;             // 16 KB
+constexpr uint32_t kTileBBytes = kBN * kBK * 2;             // 32 KB
+constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes; // 48 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;                         // 2 accumulators x 256 fp32 columns
+constexpr uint32_t kNumBars = 2 * kStages + 5;              // full, empty, tfull x2, tempty x2, drain
+constexpr size_t kGemmSmem = 1024 + size_t(kStages) * kStageBytes + 8 * kNumBars + 16;
+
+static_assert(kBM == 128 && kBN == 256 && kBK == 64, "tile shape baked into the descriptors");
+
+template <int PHASE, bool LAST>
+__global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ NsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + uint32_t(kStages) * kStageBytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + size_t(kStages) * kStageBytes + 8 * kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto full_bar = [&](int s) { return bars + 8u * uint32_t(s); };
+  auto empty_bar = [&](int s) { return bars + 8u * uint32_t(kStages + s); };
+  auto tfull_bar = [&](int s) { return bars + 8u * uint32_t(2 * kStages + s); };
+  auto tempty_bar = [&](int s) { return bars + 8u * uint32_t(2 * kStages + 2 + s); };
+  const uint32_t drain_bar = bars + 8u * uint32_t(2 * kStages + 4);
+
+  const int warp = int(threadIdx.x >> 5);
+  const int lane = int(threadIdx.x & 31);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(tfull_bar(s), 1);
+      ptx::mbar_init(tempty_bar(s), 128);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int32_t pending[kStages];
+      for (int s = 0; s < kStages; ++s) pending[s] = -1;
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      uint32_t last_mat = 0xFFFFFFFFu;
+      for (int t = int(blockIdx.x); ok && t < p.ntiles; t += int(gridDim.x)) {
+        const TileRec tr = p.tiles[t];
+        const DevMat& M = p.mats[tr.mat];
+        const CUtensorMap* maps = p.tmaps + size_t(tr.mat) * kMapsPerMat;
+        const void* mapA;
+        const void* mapB;
+        int K;
+        if (PHASE == MO_PHASE_GRAM) {
+          mapA = mapB = &maps[p.cur];
+          K = M.n;
+        } else if (PHASE == MO_PHASE_POLY) {
+          mapA = mapB = &maps[2];
+          K = M.m;
+        } else {
+          mapA = &maps[3];
+          mapB = &maps[p.cur];
+          K = M.m;
+        }
+        const int nk = (K + kBK - 1) / kBK;
+        const int row0 = int(tr.tm) * kBM;
+        const int col0 = int(tr.tn) * kBN;
+        if (tr.mat != last_mat) {
+          ptx::fence_tmap_acquire(mapA);
+          ptx::fence_tmap_acquire(mapB);
+          last_mat = tr.mat;
+        }
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint32_t sa = base + uint32_t(stage) * kStageBytes;
+          const uint32_t sb = sa + kTileABytes;
+          const int k0 = kb * kBK;
+          ptx::tma_load_2d(sa, mapA, fb, k0, row0);
+          ptx::tma_load_2d(sa + kBoxBytes, mapA, fb, k0, row0 + 64);
+          if (PHASE != MO_PHASE_UPDATE) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ptx::tma_load_2d(sb + q * kBoxBytes, mapB, fb, k0, col0 + 64 * q);
+          } else {
+            // B operand X[k0:k0+64, col0:col0+256] in MN-major boxes of 64 columns
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ptx::tma_load_2d(sb + q * kBoxBytes, mapB, fb, col0 + 64 * q, k0);
+          }
+          pending[stage] = int32_t(ph);
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // never leave the CTA with bulk copies still landing in its shared memory
+        for (int s = 0; s < kStages; ++s)
+          if (pending[s] >= 0) mbar_wait_drain(full_bar(s), uint32_t(pending[s]), p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc =
+          ptx::idesc_bf16_f32(kBM, kBN, 0u, PHASE == MO_PHASE_UPDATE ? 1u : 0u);
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      bool issued = false;
+      bool ok = true;
+      for (int t = int(blockIdx.x); ok && t < p.ntiles; t += int(gridDim.x)) {
+        const TileRec tr = p.tiles[t];
+        const DevMat& M = p.mats[tr.mat];
+        const int K = (PHASE == MO_PHASE_GRAM) ? M.n : M.m;
+        const int nk = (K + kBK - 1) / kBK;
+        if (!mbar_wait_bounded(tempty_bar(acc), aph ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc) * uint32_t(kBN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), ph, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = base + uint32_t(stage) * kStageBytes;
+          const uint32_t sb = sa + kTileABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(sa + uint32_t(kk) * 32u, 16u, 1024u);
+            const uint64_t bd = (PHASE == MO_PHASE_UPDATE)
+                                    ? ptx::smem_desc_sw128(sb + uint32_t(kk) * 2048u, kBoxBytes, 1024u)
+                                    : ptx::smem_desc_sw128(sb + uint32_t(kk) * 32u, 16u, 1024u);
+            ptx::umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit(empty_bar(stage));
+          issued = true;
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::umma_commit(tfull_bar(acc));
+        acc ^= 1;
+        if (acc == 0) aph ^= 1u;
+      }
+      if (*abort_flag && issued) {
+        ptx::umma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0u, p.timeout_ns);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
+    const int r_in = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = int(blockIdx.x); t < p.ntiles; t += int(gridDim.x)) {
+      const TileRec tr = p.tiles[t];
+      const DevMat& M = p.mats[tr.mat];
+      bool ok = mbar_wait_bounded(tfull_bar(acc), aph, abort_flag, p.status, p.timeout_ns);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int row = int(tr.tm) * kBM + r_in;
+      const uint32_t tb = tmem_base + uint32_t(acc) * uint32_t(kBN) + (uint32_t(quarter * 32) << 16);
+#pragma unroll 1
+      for (int ch = 0; ch < kBN / 32; ++ch) {
+        uint32_t r[32];
+        __syncwarp();
+        ptx::tmem_ld_32x32b_x32(tb + uint32_t(ch * 32), r);
+        ptx::tmem_ld_wait();
+        const int col0 = int(tr.tn) * kBN + ch * 32;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        if (PHASE == MO_PHASE_GRAM || PHASE == MO_PHASE_POLY) {
+          const int m = M.m;
+          if (row < m && col0 < m) {
+            uint16_t* out = (PHASE == MO_PHASE_GRAM) ? M.A : M.B;
+            const size_t ld = size_t(M.lda);
+            const bool full_chunk = col0 + 32 <= m;
+            if (PHASE == MO_PHASE_POLY) {
+              const uint16_t* a_row = M.A + size_t(row) * ld + col0;
+              if (full_chunk) {
+                const uint4* src = reinterpret_cast<const uint4*>(a_row);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const uint4 u = src[q];
+                  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    v[q * 8 + 2 * j] = p.b * bf16_bits_to_float(w[j] & 0xFFFFu) + p.c * v[q * 8 + 2 * j];
+                    v[q * 8 + 2 * j + 1] = p.b * bf16_bits_to_float(w[j] >> 16) + p.c * v[q * 8 + 2 * j + 1];
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + i < m) v[i] = p.b * bf16_bits_to_float(a_row[i]) + p.c * v[i];
+              }
+            }
+            // direct store of the upper part (col >= row)
+            uint16_t* o_row = out + size_t(row) * ld + col0;
+            if (full_chunk && col0 >= row) {
+              uint4* dst = reinterpret_cast<uint4*>(o_row);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                                    pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int col = col0 + i;
+                if (col >= row && col < m) o_row[i] = float_to_bf16_bits(v[i]);
+              }
+            }
+            // mirrored store of the strictly upper part into the lower triangle
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int col = col0 + i;
+              if (col > row && col < m) out[size_t(col) * ld + row] = float_to_bf16_bits(v[i]);
+            }
+          }
+        } else {
+          const int m = M.m, n = M.n;
+          if (row < m && col0 < n) {
+            const bool full_chunk = col0 + 32 <= n;
+            const uint16_t* x_row = M.X[p.cur] + size_t(row) * size_t(M.ldx) + col0;
+            float x[32];
+            if (full_chunk) {
+              const uint4* src = reinterpret_cast<const uint4*>(x_row);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 u = src[q];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  x[q * 8 + 2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
+                  x[q * 8 + 2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) x[i] = (col0 + i < n) ? bf16_bits_to_float(x_row[i]) : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = fmaf(p.a, x[i], v[i]);
+            if (!LAST) {
+              uint16_t* o_row = M.X[p.cur ^ 1] + size_t(row) * size_t(M.ldx) + col0;
+              if (full_chunk) {
+                uint4* dst = reinterpret_cast<uint4*>(o_row);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  dst[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                                      pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + i < n) o_row[i] = float_to_bf16_bits(v[i]);
+              }
+            } else {
+              const float decay = p.decay;
+              const float step = p.lr * M.shape_scale;
+              if (!M.tall) {
+                // W is [m, n]: element (row, col)
+                float* w_row = M.W + size_t(row) * size_t(M.C) + col0;
+                if (full_chunk && M.vec_ok) {
+                  float4* wp = reinterpret_cast<float4*>(w_row);
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) {
+                    float4 w4 = wp[q];
+                    w4.x = w4.x * decay - step * v[4 * q + 0];
+                    w4.y = w4.y * decay - step * v[4 * q + 1];
+                    w4.z = w4.z * decay - step * v[4 * q + 2];
+                    w4.w = w4.w * decay - step * v[4 * q + 3];
+                    wp[q] = w4;
+                  }
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    if (col0 + i < n) w_row[i] = w_row[i] * decay - step * v[i];
+                }
+              } else {
+                // W is [n, m]: element (col, row); lanes hold consecutive rows
+                float* w_col = M.W + size_t(col0) * size_t(M.C) + row;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + i < n) {
+                    float* w = w_col + size_t(i) * size_t(M.C);
+                    *w = *w * decay - step * v[i];
+                  }
+              }
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// Single-CTA kernel that waits on a barrier nothing completes; exercises the
+// bounded-wait path.
+__global__ void bounded_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_addr(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    mbar_wait_bounded(ptx::smem_addr(&bar), 0u, reinterpret_cast<volatile int*>(&abort_flag), status,
+                      timeout_ns);
+  __syncthreads();
+}
+
+template <int PHASE, bool LAST>
+cudaError_t launch_one(const NsParams& p, int grid, cudaStream_t stream) {
+  auto kern = ns_gemm_kernel<PHASE, LAST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemmSmem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, kGemmSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t ns_gemm_smem_bytes() { return kGemmSmem; }
+
+cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream) {
+  if (p.ntiles <= 0) return cudaSuccess;
+  switch (phase) {
+    case MO_PHASE_GRAM:
+      return launch_one<MO_PHASE_GRAM, false>(p, grid, stream);
+    case MO_PHASE_POLY:
+      return launch_one<MO_PHASE_POLY, false>(p, grid, stream);
+    default:
+      return last ? launch_one<MO_PHASE_UPDATE, true>(p, grid, stream)
+                  : launch_one<MO_PHASE_UPDATE, false>(p, grid, stream);
+  }
+}
+
+cudaError_t device_status_ptr(int** out) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_mo_status);
+}
+
+cudaError_t launch_bounded_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool encode_bf16_2d(CUtensorMap* map, void* gaddr, uint64_t cols, uint64_t rows, uint64_t ld_elems) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld_elems * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gaddr, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool encode_matrix_maps(const DevMat& d, void* out_maps) {
+  static_assert(sizeof(CUtensorMap) == kTensorMapBytes, "CUtensorMap size");
+  CUtensorMap* maps = static_cast<CUtensorMap*>(out_maps);
+  return encode_bf16_2d(&maps[0], d.X[0], uint64_t(d.n), uint64_t(d.m), uint64_t(d.ldx)) &&
+         encode_bf16_2d(&maps[1], d.X[1], uint64_t(d.n), uint64_t(d.m), uint64_t(d.ldx)) &&
+         encode_bf16_2d(&maps[2], d.A, uint64_t(d.m), uint64_t(d.m), uint64_t(d.lda)) &&
+         encode_bf16_2d(&maps[3], d.B, uint64_t(d.m), uint64_t(d.m), uint64_t(d.lda));
+}
+
+}  // namespace mo

@@ -1,0 +1,43 @@
+// Host-only planning: argument validation, Newton-Schulz tile schedules and
+// the Muon workspace layout. No CUDA calls, so all of it runs (and is tested)
+// on a machine without a GPU.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "mo_internal.h"
+
+namespace mo {
+
+struct MuonLayout {
+  int32_t n = 0;
+  std::vector<DevMat> mats;          // buffer pointers hold workspace OFFSETS until bound
+  std::vector<int64_t> nrm_prefix;   // n + 1 prefix sums of sum-of-squares chunks
+  std::vector<int64_t> cast_prefix;  // n + 1 prefix sums of normalise/cast tiles
+  std::vector<TileRec> tiles[3];     // per phase, launch order
+  int64_t nrm_total = 0;
+  int64_t cast_total = 0;
+  size_t off_meta = 0, off_tmaps = 0, off_nrm_prefix = 0, off_cast_prefix = 0, off_counters = 0;
+  size_t off_tiles[3] = {0, 0, 0};
+  size_t header_bytes = 0;           // [0, header_bytes) is uploaded by every call
+  size_t off_partials = 0, off_scales = 0, off_buffers = 0;
+  size_t total_bytes = 0;
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int validate_matrix_table(const mo_matrix* tbl, int32_t n);
+int validate_muon_params(const mo_muon_params* p);
+int validate_rmnp_params(const mo_rmnp_params* p);
+int validate_adamw(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* p);
+
+// Tile schedule of one phase (MO_PHASE_*), sorted into launch order.
+void build_tiles(const mo_matrix* tbl, int32_t n, int phase, std::vector<TileRec>& out);
+
+// Layout of the Muon workspace for a validated table.
+void plan_muon(const mo_matrix* tbl, int32_t n, MuonLayout& L);
+
+}  // namespace mo

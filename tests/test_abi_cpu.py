@@ -1,0 +1,186 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every
+function include/mo.h declares; validation rejects bad arguments before any
+CUDA call; the tile schedules are bit-exact against a plain Python restatement
+of their rules and cover every output element exactly once."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import matrix_optimizers_zero_gb300 as mo
+from matrix_optimizers_zero_gb300 import build as mo_build
+from matrix_optimizers_zero_gb300 import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mo_build.build()
+    return mo.load_library()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "mo.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert "muon_owner_step" in names and "adamw_tail_step" in names and "rmnp_step" in names
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.mo_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -9]:
+        s = mo.mo_status_string(code)
+        assert s and s != "unknown status"
+    assert mo.mo_status_string(12345) == "unknown status"
+
+
+# ---------------------------------------------------------------- schedules
+
+def py_schedule(shapes, phase):
+    keys = []
+    for i, (R, C) in enumerate(shapes):
+        m, n = min(R, C), max(R, C)
+        tiles_m = -(-m // 128)
+        if phase == mo.PHASE_UPDATE:
+            for tm in range(tiles_m):
+                for tn in range(-(-n // 256)):
+                    keys.append((-m, i, tm, tn))
+        else:
+            k = n if phase == mo.PHASE_GRAM else m
+            for tm in range(tiles_m):
+                for tn in range(-(-m // 256)):
+                    if (tn + 1) * 256 > tm * 128:
+                        keys.append((-k, i, tm, tn))
+    keys.sort()
+    return [(i, tm, tn) for _, i, tm, tn in keys]
+
+
+TABLES = {
+    "gpt2l": [(s.rows, s.cols) for s in workloads.get_workload("gpt2l").matrices],
+    "share32b": [(s.rows, s.cols) for s in workloads.get_workload("share32b").matrices],
+    "ragged": [(130, 257), (257, 130), (1, 9), (9, 1), (128, 256), (300, 300), (1000, 70)],
+}
+
+
+@pytest.mark.parametrize("table", sorted(TABLES))
+@pytest.mark.parametrize("phase", [0, 1, 2])
+def test_schedule_bit_exact(lib, table, phase):
+    shapes = TABLES[table]
+    assert mo.mo_muon_tile_schedule(shapes, phase) == py_schedule(shapes, phase)
+
+
+@pytest.mark.parametrize("shape", [(130, 257), (257, 130), (300, 300), (700, 1500), (1, 5)])
+def test_schedule_covers_outputs_exactly_once(lib, shape):
+    m, n = min(shape), max(shape)
+    for phase in (0, 1):
+        cover = np.zeros((m, m), dtype=np.int32)
+        for _, tm, tn in mo.mo_muon_tile_schedule([shape], phase):
+            r0, c0 = tm * 128, tn * 256
+            # the epilogue's store rule: direct for col >= row, mirror for col > row
+            for r in range(r0, min(r0 + 128, m)):
+                for c in range(c0, min(c0 + 256, m)):
+                    if c >= r:
+                        cover[r, c] += 1
+                    if c > r:
+                        cover[c, r] += 1
+        assert np.all(cover == 1), phase
+    cover = np.zeros((m, n), dtype=np.int32)
+    for _, tm, tn in mo.mo_muon_tile_schedule([shape], 2):
+        cover[tm * 128:tm * 128 + 128, tn * 256:tn * 256 + 256] += 1
+    assert np.all(cover == 1)
+
+
+def test_workspace_bytes(lib):
+    shapes = [(130, 257), (257, 130)]
+    arr = mo.fake_table(shapes)
+    p = mo.MuonParams()
+    nb = lib.mo_muon_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), 2, ctypes.byref(p))
+    # lower bound: two bf16 iterates and A, B per matrix with 64-element padded rows
+    lower = sum(2 * min(s) * (-(-max(s) // 64) * 64) * 2 + 2 * min(s) * (-(-min(s) // 64) * 64) * 2 for s in shapes)
+    assert nb >= lower and nb < lower + 64 * 1024
+    bad = mo.MuonParams(ns_steps=0)
+    assert lib.mo_muon_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), 2, ctypes.byref(bad)) == 0
+    g = [(s.rows, s.cols) for s in workloads.get_workload("gpt2l").matrices]
+    big = mo.fake_table(g)
+    nb2 = lib.mo_muon_workspace_bytes(ctypes.cast(big, ctypes.c_void_p), len(g), ctypes.byref(p))
+    buffers = sum(2 * min(r, c) * max(r, c) * 2 + 2 * min(r, c) ** 2 * 2 for r, c in g)
+    assert buffers <= nb2 < buffers * 1.01
+
+
+# ---------------------------------------------------------------- validation (no GPU needed)
+
+def _muon(lib, arr, n, params, ws=1 << 30, ws_bytes=1 << 40):
+    return lib.muon_owner_step(ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None, n,
+                               ctypes.byref(params), ws, ws_bytes, None)
+
+
+def test_muon_validation_codes(lib):
+    p = mo.MuonParams()
+    ok = mo.fake_table([(16, 32)])
+    assert _muon(lib, None, 1, p) == -1                        # null table
+    assert _muon(lib, ok, -1, p) == -2
+    assert _muon(lib, None, 0, p) == 0                          # empty table is a no-op
+    zero = mo.fake_table([(16, 32)])
+    zero[0].rows = 0
+    assert _muon(lib, zero, 1, p) == -2
+    mis = mo.fake_table([(16, 32)])
+    mis[0].W += 4
+    assert _muon(lib, mis, 1, p) == -3
+    nulls = mo.fake_table([(16, 32)])
+    nulls[0].V = None
+    assert _muon(lib, nulls, 1, p) == -1
+    over = mo.fake_table([(16, 32)])
+    over[0].V = over[0].W + 16
+    assert _muon(lib, over, 1, p) == -6
+    alias = mo.fake_table([(16, 32)])
+    alias[0].G = alias[0].W
+    assert _muon(lib, alias, 1, p) == -6
+    two = mo.fake_table([(16, 32), (16, 32)])
+    two[1].W = two[0].V
+    assert _muon(lib, two, 2, p) == -6
+    for bad in (mo.MuonParams(lr=float("nan")), mo.MuonParams(ns_steps=0), mo.MuonParams(ns_steps=101),
+                mo.MuonParams(eps=-1.0), mo.MuonParams(a=float("inf"))):
+        assert _muon(lib, ok, 1, bad) == -4
+    assert _muon(lib, ok, 1, p, ws=0) == -1
+    assert _muon(lib, ok, 1, p, ws=(1 << 30) + 16) == -3
+    assert _muon(lib, ok, 1, p, ws_bytes=1024) == -5
+    big = mo.fake_table([(70000, 70000)])
+    assert _muon(lib, big, 1, p) == -2                          # m above the supported maximum
+
+
+def test_adamw_and_rmnp_validation_codes(lib):
+    seg = (mo.MoTailSeg * 1)()
+    seg[0] = mo.MoTailSeg(1 << 20, 2 << 20, 3 << 20, 4 << 20, 1000)
+    sp = ctypes.cast(seg, ctypes.c_void_p)
+    assert lib.adamw_tail_step(sp, 1, ctypes.byref(mo.AdamWParams(step=0)), None) == -4
+    assert lib.adamw_tail_step(sp, 1, ctypes.byref(mo.AdamWParams(beta1=1.0)), None) == -4
+    assert lib.adamw_tail_step(sp, 1, ctypes.byref(mo.AdamWParams(eps=float("nan"))), None) == -4
+    assert lib.adamw_tail_step(None, 1, ctypes.byref(mo.AdamWParams()), None) == -1
+    assert lib.adamw_tail_step(None, 0, ctypes.byref(mo.AdamWParams()), None) == 0
+    seg[0].m = seg[0].p + 8 * 16
+    assert lib.adamw_tail_step(sp, 1, ctypes.byref(mo.AdamWParams()), None) == -6
+    seg[0].m = (3 << 20) + 4
+    assert lib.adamw_tail_step(sp, 1, ctypes.byref(mo.AdamWParams()), None) == -3
+    seg[0].m = 3 << 20
+    seg[0].g = seg[0].v
+    assert lib.adamw_tail_step(sp, 1, ctypes.byref(mo.AdamWParams()), None) == -6
+
+    t = mo.fake_table([(16, 32)])
+    tp = ctypes.cast(t, ctypes.c_void_p)
+    assert lib.rmnp_step(tp, 1, ctypes.byref(mo.RmnpParams(eps=-1.0)), None) == -4
+    assert lib.rmnp_step(None, 0, ctypes.byref(mo.RmnpParams()), None) == 0
+    assert lib.rmnp_step_scaled(tp, None, 1, ctypes.byref(mo.RmnpParams()), None) == -1
+    sc = (ctypes.c_float * 1)(float("nan"))
+    assert lib.rmnp_step_scaled(tp, ctypes.cast(sc, ctypes.c_void_p), 1, ctypes.byref(mo.RmnpParams()), None) == -4
