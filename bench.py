@@ -107,11 +107,11 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def cpu_oracle_sample(wl, max_seconds=20.0, indices=None):
+def cpu_oracle_sample(wl, max_seconds=20.0, indices=None, min_seconds=0.0):
     """Times the CPU oracle (as it stands) on a bounded sample of the
     workload: whole-matrix Muon steps on one matrix per distinct shape, in
-    table order, until max_seconds is spent. Returns (TFLOP/s, seconds,
-    description, cores)."""
+    table order (repeated until min_seconds of work), stopping once
+    max_seconds is spent. Returns (TFLOP/s, seconds, description, cores)."""
     import numpy as np
     import oracle
     from matrix_optimizers_zero_gb300 import workloads
@@ -126,7 +126,10 @@ def cpu_oracle_sample(wl, max_seconds=20.0, indices=None):
     flops = 0
     t_total = 0.0
     done = []
-    for i in picks:
+    order = list(picks) * (8 if min_seconds > 0 else 1)
+    for k, i in enumerate(order):
+        if k >= len(picks) and t_total >= min_seconds:
+            break
         W, G, V = workloads.host_matrix(wl, i, v_std=1e-3)
         W, G, V = (t.float().double().numpy() for t in (W, G, V))
         t0 = time.perf_counter()
@@ -244,6 +247,10 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for e in evs:
+        for x in e:
+            x.record(stream)          # torch creates events lazily: force the handles to exist
+    torch.cuda.synchronize(dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -279,14 +286,16 @@ def run_ours(args, rank, world, local_rank):
     value = world * ns_flops / (ms_max * 1e-3) / 1e12
 
     # ---- end to end through the C ABI with host buffers
-    e2e_steps = max(1, min(args.steps, 10))
-    hG = torch.empty(Gf.numel(), dtype=torch.bfloat16, pin_memory=True)
-    hG.copy_(Gf)
-    hTg = torch.empty(Tg.numel(), dtype=torch.float32, pin_memory=True)
-    hTg.copy_(Tg)
-    hW = torch.empty(Wf.numel(), dtype=torch.float32, pin_memory=True)
-    hWr = torch.empty(Wr.numel(), dtype=torch.float32, pin_memory=True)
-    hP = torch.empty(Pf.numel(), dtype=torch.float32, pin_memory=True)
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 10))
+    pin = e2e_steps > 0
+    hG = torch.empty(Gf.numel() if pin else 1, dtype=torch.bfloat16, pin_memory=pin)
+    hTg = torch.empty(Tg.numel() if pin else 1, dtype=torch.float32, pin_memory=pin)
+    hW = torch.empty(Wf.numel() if pin else 1, dtype=torch.float32, pin_memory=pin)
+    hWr = torch.empty(Wr.numel() if pin else 1, dtype=torch.float32, pin_memory=pin)
+    hP = torch.empty(Pf.numel() if pin else 1, dtype=torch.float32, pin_memory=pin)
+    if pin:
+        hG.copy_(Gf)
+        hTg.copy_(Tg)
     h2d = hG.numel() * 2 + hTg.numel() * 4
     d2h = hW.numel() * 4 + hWr.numel() * 4 + hP.numel() * 4
     barrier()
@@ -302,7 +311,7 @@ def run_ours(args, rank, world, local_rank):
         hP.copy_(Pf, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = e0.elapsed_time(e1) / max(e2e_steps, 1)
     t_e2e = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
     if dist is not None:
         dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
@@ -360,13 +369,14 @@ def run_ours(args, rank, world, local_rank):
             "traffic": None,
             "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
         },
-        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(float(t_e2e.item()), 3)},
+        "e2e": ({"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(float(t_e2e.item()), 3)}
+                if e2e_steps else None),
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
-        v, secs, desc, cores = cpu_oracle_sample(wl, max_seconds=args.cpu_seconds)
+        v, secs, desc, cores = cpu_oracle_sample(wl, max_seconds=args.cpu_seconds, min_seconds=10.0)
         out["cpu_baseline"] = {"value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": desc, "seconds": round(secs, 2)}
     return out
@@ -416,8 +426,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="gpt2l")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=25.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

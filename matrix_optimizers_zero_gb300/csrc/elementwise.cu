@@ -1,6 +1,6 @@
-// Memory-bound kernels of the owner-local step: the fused Muon prologue
-// (momentum + Frobenius sum of squares + bf16 cast/transpose), RMNP and
-// AdamW. All accesses along rows are 16-byte vectors where the row length
+// Memory-bound kernels of the owner-local step: the two Muon prologue passes
+// (momentum + Frobenius sum of squares; normalise + bf16 cast/transpose), RMNP
+// and AdamW. All accesses along rows are 16-byte vectors where the row length
 // allows it; every kernel is a grid-stride loop over a flat work list sized to
 // a multiple of the SM count.
 #include <cuda_runtime.h>
@@ -27,7 +27,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // matrix's partials in a fixed order (deterministic, no float atomics) and
 // writes the Frobenius scale 1 / (||V|| + eps) (the appendix of the same page:
 // eps is added to the norm).
-__global__ void __launch_bounds__(256) muon_momentum_norm_kernel(const __grid_constant__ ProParams p) {
+__global__ void __launch_bounds__(256, 4) muon_momentum_norm_kernel(const __grid_constant__ ProParams p) {
   __shared__ float red[8];
   __shared__ int last_flag;
   const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
@@ -39,16 +39,17 @@ __global__ void __launch_bounds__(256) muon_momentum_norm_kernel(const __grid_co
     }
     const int mi = lo;
     const DevMat& M = p.mats[mi];
-    const int64_t total = int64_t(M.R) * int64_t(M.C);
     const int64_t e0 = (t - p.nrm_prefix[mi]) * kNrmChunk;
-    float* __restrict__ V = M.V;
-    const uint16_t* __restrict__ G = M.G;
+    const int64_t left = int64_t(M.R) * int64_t(M.C) - e0;
+    const int cnt = left < kNrmChunk ? int(left) : int(kNrmChunk);   // elements in this chunk
+    float* __restrict__ V = M.V + e0;
+    const uint16_t* __restrict__ G = M.G + e0;
     float4 v[8];
     uint2 g[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int64_t e = e0 + int64_t(j * 256 + tid) * 4;
-      if (e + 4 <= total) {
+      const int e = (j * 256 + tid) * 4;
+      if (e + 4 <= cnt) {
         v[j] = *reinterpret_cast<const float4*>(V + e);
         g[j] = *reinterpret_cast<const uint2*>(G + e);
       }
@@ -56,8 +57,8 @@ __global__ void __launch_bounds__(256) muon_momentum_norm_kernel(const __grid_co
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int64_t e = e0 + int64_t(j * 256 + tid) * 4;
-      if (e + 4 <= total) {
+      const int e = (j * 256 + tid) * 4;
+      if (e + 4 <= cnt) {
         float4 n4;
         n4.x = fmaf(p.mu, v[j].x, bf16_bits_to_float(g[j].x & 0xFFFFu));
         n4.y = fmaf(p.mu, v[j].y, bf16_bits_to_float(g[j].x >> 16));
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(256) muon_momentum_norm_kernel(const __grid_co
         ss = fmaf(n4.z, n4.z, ss);
         ss = fmaf(n4.w, n4.w, ss);
       } else {
-        for (int64_t k = e; k < total && k < e + 4; ++k) {
+        for (int k = e; k < cnt && k < e + 4; ++k) {
           const float vn = fmaf(p.mu, V[k], bf16_bits_to_float(G[k]));
           V[k] = vn;
           ss = fmaf(vn, vn, ss);
@@ -127,50 +128,54 @@ __global__ void __launch_bounds__(256) muon_normalize_cast_kernel(const __grid_c
     const int r0 = int(local / M.cast_tiles_c) * kCastTR;
     const int c0 = int(local % M.cast_tiles_c) * kCastTC;
     const int R = M.R, C = M.C;
-    const int cl = lane * 4;
-    const int c = c0 + cl;
-    const bool tall = M.tall != 0;
     const float sc = p.scales[mi];
     uint16_t* X = M.X[0];
     const size_t ldx = size_t(M.ldx);
+    if (!M.tall) {
+      // warp w covers rows w, w+8, ...; lanes cover 4 consecutive columns each
+      const int c = c0 + lane * 4;
 #pragma unroll 4
-    for (int i = 0; i < kCastTR / 8; ++i) {
-      const int rl = warp + 8 * i;
-      const int r = r0 + rl;
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
-      if (r < R && c < C) {
+      for (int i = 0; i < kCastTR / 8; ++i) {
+        const int r = r0 + warp + 8 * i;
+        if (r >= R || c >= C) continue;
         const size_t off = size_t(r) * size_t(C) + size_t(c);
+        uint16_t* xp = X + size_t(r) * ldx + size_t(c);
         if (M.vec_ok && c + 4 <= C) {
           const float4 v4 = *reinterpret_cast<const float4*>(M.V + off);
-          x[0] = v4.x * sc;
-          x[1] = v4.y * sc;
-          x[2] = v4.z * sc;
-          x[3] = v4.w * sc;
+          *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16x2(v4.x * sc, v4.y * sc), pack_bf16x2(v4.z * sc, v4.w * sc));
         } else {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (c + q < C) x[q] = M.V[off + q] * sc;
+            if (c + q < C) xp[q] = float_to_bf16_bits(M.V[off + q] * sc);
         }
       }
-      if (!tall) {
-        if (r < R && c < C) {
-          uint16_t* xp = X + size_t(r) * ldx + size_t(c);
-          if (c + 4 <= C) {
-            *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
-          } else {
+    } else {
+      // X is [C, R]: X[c][r] = bf16(V[r][c] * scale). Thread = (row rl, 32-column
+      // quarter cq): lanes hold consecutive rows, so the shared-memory writes
+      // tbuf[c][rl] of a warp are contiguous.
+      const int rl = tid & (kCastTR - 1);
+      const int cq = tid >> 6;
+      const int r = r0 + rl;
+      const int cb = cq * 32;
+      if (r < R) {
+        const float* vrow = M.V + size_t(r) * size_t(C) + size_t(c0 + cb);
+        if (M.vec_ok && c0 + cb + 32 <= C) {
+          float4 v4[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (c + q < C) xp[q] = float_to_bf16_bits(x[q]);
+          for (int j = 0; j < 8; ++j) v4[j] = reinterpret_cast<const float4*>(vrow)[j];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            tbuf[cb + 4 * j + 0][rl] = float_to_bf16_bits(v4[j].x * sc);
+            tbuf[cb + 4 * j + 1][rl] = float_to_bf16_bits(v4[j].y * sc);
+            tbuf[cb + 4 * j + 2][rl] = float_to_bf16_bits(v4[j].z * sc);
+            tbuf[cb + 4 * j + 3][rl] = float_to_bf16_bits(v4[j].w * sc);
           }
+        } else {
+          for (int j = 0; j < 32; ++j) tbuf[cb + j][rl] = (c0 + cb + j < C) ? float_to_bf16_bits(vrow[j] * sc) : uint16_t(0);
         }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tbuf[cl + q][rl] = float_to_bf16_bits(x[q]);
       }
-    }
-    if (tall) {
       __syncthreads();
-      // X is [C, R]: X[c][r] = bf16(V[r][c] * scale); 16-byte segments of 8 rows
+      // 16-byte segments of 8 rows per X row
       for (int k = tid; k < kCastTC * (kCastTR / 8); k += 256) {
         const int cc = k >> 3, seg = k & 7;
         const int xc = c0 + cc;

@@ -10,13 +10,13 @@
 //                                    W <- W (1 - lr wd) - lr s X' instead)
 // X0 = bf16(V / (||V||_F + eps)) is written by the prologue.
 //
-// Kernel structure (one persistent CTA per SM, 6 warps):
+// Kernel structure (one persistent CTA per SM, 10 warps):
 //   warp 0      TMA producer: 128x64 A-operand and 256x64 B-operand boxes
 //               (128-byte swizzle) into a 4-stage shared-memory ring
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //               (M=128, N=256, K=16 per instruction, fp32 accumulate)
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane per
-//               thread), fused arithmetic, bf16/fp32 stores
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator (one TMEM lane and
+//               128 columns per thread), fused arithmetic, bf16/fp32 stores
 // The two 256-column accumulators in TMEM let the epilogue of one tile run
 // under the main loop of the next.
 #include <cuda.h>
@@ -42,12 +42,193 @@ constexpr uint32_t kBoxBytes = 64 * 64 * 2;                 // one TMA box: 64 x
 constexpr uint32_t kTileABytes = kBM * kBK * 2;             // 16 KB
 constexpr uint32_t kTileBBytes = kBN * kBK * 2;             // 32 KB
 constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes; // 48 KB
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                                 // two per TMEM lane quarter
+constexpr int kEpiCols = kBN / 2;                            // accumulator columns per epilogue thread
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;                         // 2 accumulators x 256 fp32 columns
 constexpr uint32_t kNumBars = 2 * kStages + 5;              // full, empty, tfull x2, tempty x2, drain
 constexpr size_t kGemmSmem = 1024 + size_t(kStages) * kStageBytes + 8 * kNumBars + 16;
 
 static_assert(kBM == 128 && kBN == 256 && kBK == 64, "tile shape baked into the descriptors");
+
+// ------------------------------------------------------------------ epilogues
+// Each epilogue thread owns one accumulator row (TMEM lane) and kEpiCols
+// consecutive columns of it, processed in chunks of 32. Operand loads for the
+// next chunk are issued before the current chunk's accumulator is read, and
+// every load of a chunk is issued before its stores.
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* x) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
+    x[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+  }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
+// Loads the 32 bf16 values of `row_ptr[col0 .. col0+32)` as four 16-byte
+// vectors when the whole chunk is inside the row (valid = row in range).
+__device__ __forceinline__ void prefetch_chunk(const uint16_t* row_ptr, int col0, int ncols, bool valid,
+                                               uint4 (&dst)[4]) {
+  if (valid && col0 + 32 <= ncols) {
+    const uint4* src = reinterpret_cast<const uint4*>(row_ptr + col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = src[q];
+  }
+}
+
+__device__ __forceinline__ void chunk_operand(const uint16_t* row_ptr, int col0, int ncols,
+                                              const uint4 (&pre)[4], float (&x)[32]) {
+  if (col0 + 32 <= ncols) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) unpack_bf16x8(pre[q], &x[q * 8]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = (col0 + i < ncols) ? bf16_bits_to_float(row_ptr[col0 + i]) : 0.0f;
+  }
+}
+
+__device__ __forceinline__ void tmem_chunk(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  __syncwarp();
+  ptx::tmem_ld_32x32b_x32(taddr, r);
+  ptx::tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// GRAM: A = acc.  POLY: B = b A + c acc.  Stored bf16 to the upper triangle
+// (col >= row) and mirrored to the strict lower triangle, so every element of
+// the symmetric result is written exactly once.
+template <int PHASE>
+__device__ __forceinline__ void epilogue_symmetric(const NsParams& p, const DevMat& M, int row, int cbase,
+                                                   uint32_t tb) {
+  const int m = M.m;
+  const size_t ld = size_t(M.lda);
+  const bool rv = row < m;
+  uint16_t* out = (PHASE == MO_PHASE_GRAM) ? M.A : M.B;
+  const uint16_t* a_row = M.A + size_t(rv ? row : 0) * ld;
+  uint4 pre[4], nxt[4];
+  if (PHASE == MO_PHASE_POLY) prefetch_chunk(a_row, cbase, m, rv, nxt);
+#pragma unroll 1
+  for (int ch = 0; ch < kEpiCols / 32; ++ch) {
+    const int col0 = cbase + ch * 32;
+    if (PHASE == MO_PHASE_POLY) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) pre[q] = nxt[q];
+      if (ch + 1 < kEpiCols / 32) prefetch_chunk(a_row, col0 + 32, m, rv, nxt);
+    }
+    float v[32];
+    tmem_chunk(tb + uint32_t(ch * 32), v);
+    if (!rv || col0 >= m) continue;
+    if (PHASE == MO_PHASE_POLY) {
+      float a[32];
+      chunk_operand(a_row, col0, m, pre, a);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = fmaf(p.b, a[i], p.c * v[i]);
+    }
+    uint16_t* o_row = out + size_t(row) * ld + col0;
+    if (col0 + 32 <= m && col0 >= row) {
+      uint4* dst = reinterpret_cast<uint4*>(o_row);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = pack_bf16x8(&v[q * 8]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i >= row && col0 + i < m) o_row[i] = float_to_bf16_bits(v[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int col = col0 + i;
+      if (col > row && col < m) out[size_t(col) * ld + row] = float_to_bf16_bits(v[i]);
+    }
+  }
+}
+
+// UPDATE: X' = a X + acc (bf16 to the other X buffer), or in the last
+// iteration W <- W decay - lr s X' on the stored orientation.
+template <bool LAST>
+__device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat& M, int row, int cbase,
+                                                uint32_t tb) {
+  const int m = M.m, n = M.n;
+  const bool rv = row < m;
+  const uint16_t* x_row = M.X[p.cur] + size_t(rv ? row : 0) * size_t(M.ldx);
+  uint4 pre[4], nxt[4];
+  prefetch_chunk(x_row, cbase, n, rv, nxt);
+#pragma unroll 1
+  for (int ch = 0; ch < kEpiCols / 32; ++ch) {
+    const int col0 = cbase + ch * 32;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) pre[q] = nxt[q];
+    if (ch + 1 < kEpiCols / 32) prefetch_chunk(x_row, col0 + 32, n, rv, nxt);
+    float v[32];
+    tmem_chunk(tb + uint32_t(ch * 32), v);
+    if (!rv || col0 >= n) continue;
+    const bool full = col0 + 32 <= n;
+    {
+      float x[32];
+      chunk_operand(x_row, col0, n, pre, x);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = fmaf(p.a, x[i], v[i]);
+    }
+    if (!LAST) {
+      uint16_t* o_row = M.X[p.cur ^ 1] + size_t(row) * size_t(M.ldx) + col0;
+      if (full) {
+        uint4* dst = reinterpret_cast<uint4*>(o_row);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = pack_bf16x8(&v[q * 8]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < n) o_row[i] = float_to_bf16_bits(v[i]);
+      }
+    } else {
+      const float decay = p.decay;
+      const float step = p.lr * M.shape_scale;
+      if (!M.tall) {
+        // W is [m, n]: element (row, col)
+        float* w_row = M.W + size_t(row) * size_t(M.C) + col0;
+        if (full && M.vec_ok) {
+          float4* wp = reinterpret_cast<float4*>(w_row);
+          float4 w4[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) w4[q] = wp[q];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            w4[q].x = fmaf(w4[q].x, decay, -step * v[4 * q + 0]);
+            w4[q].y = fmaf(w4[q].y, decay, -step * v[4 * q + 1]);
+            w4[q].z = fmaf(w4[q].z, decay, -step * v[4 * q + 2]);
+            w4[q].w = fmaf(w4[q].w, decay, -step * v[4 * q + 3]);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) wp[q] = w4[q];
+        } else {
+          float w[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = (col0 + i < n) ? w_row[i] : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col0 + i < n) w_row[i] = fmaf(w[i], decay, -step * v[i]);
+        }
+      } else {
+        // W is [n, m]: element (col, row); the lanes of a warp hold
+        // consecutive rows, so each access below is one 128-byte line
+        float* w_col = M.W + size_t(col0) * size_t(M.C) + row;
+        float w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = (col0 + i < n) ? w_col[size_t(i) * size_t(M.C)] : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < n) w_col[size_t(i) * size_t(M.C)] = fmaf(w[i], decay, -step * v[i]);
+      }
+    }
+  }
+}
 
 template <int PHASE, bool LAST>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ NsParams p) {
@@ -74,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(tfull_bar(s), 1);
-      ptx::mbar_init(tempty_bar(s), 128);
+      ptx::mbar_init(tempty_bar(s), 32 * kEpiWarps);
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -211,7 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
+    // warps 2..9: TMEM lane quarter = warp % 4, column half = (warp - 2) / 4
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r_in = quarter * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
@@ -223,138 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       if (!ok) break;
       ptx::tc_fence_after();
       const int row = int(tr.tm) * kBM + r_in;
-      const uint32_t tb = tmem_base + uint32_t(acc) * uint32_t(kBN) + (uint32_t(quarter * 32) << 16);
-#pragma unroll 1
-      for (int ch = 0; ch < kBN / 32; ++ch) {
-        uint32_t r[32];
-        __syncwarp();
-        ptx::tmem_ld_32x32b_x32(tb + uint32_t(ch * 32), r);
-        ptx::tmem_ld_wait();
-        const int col0 = int(tr.tn) * kBN + ch * 32;
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        if (PHASE == MO_PHASE_GRAM || PHASE == MO_PHASE_POLY) {
-          const int m = M.m;
-          if (row < m && col0 < m) {
-            uint16_t* out = (PHASE == MO_PHASE_GRAM) ? M.A : M.B;
-            const size_t ld = size_t(M.lda);
-            const bool full_chunk = col0 + 32 <= m;
-            if (PHASE == MO_PHASE_POLY) {
-              const uint16_t* a_row = M.A + size_t(row) * ld + col0;
-              if (full_chunk) {
-                const uint4* src = reinterpret_cast<const uint4*>(a_row);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const uint4 u = src[q];
-                  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    v[q * 8 + 2 * j] = p.b * bf16_bits_to_float(w[j] & 0xFFFFu) + p.c * v[q * 8 + 2 * j];
-                    v[q * 8 + 2 * j + 1] = p.b * bf16_bits_to_float(w[j] >> 16) + p.c * v[q * 8 + 2 * j + 1];
-                  }
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (col0 + i < m) v[i] = p.b * bf16_bits_to_float(a_row[i]) + p.c * v[i];
-              }
-            }
-            // direct store of the upper part (col >= row)
-            uint16_t* o_row = out + size_t(row) * ld + col0;
-            if (full_chunk && col0 >= row) {
-              uint4* dst = reinterpret_cast<uint4*>(o_row);
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                                    pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int col = col0 + i;
-                if (col >= row && col < m) o_row[i] = float_to_bf16_bits(v[i]);
-              }
-            }
-            // mirrored store of the strictly upper part into the lower triangle
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int col = col0 + i;
-              if (col > row && col < m) out[size_t(col) * ld + row] = float_to_bf16_bits(v[i]);
-            }
-          }
-        } else {
-          const int m = M.m, n = M.n;
-          if (row < m && col0 < n) {
-            const bool full_chunk = col0 + 32 <= n;
-            const uint16_t* x_row = M.X[p.cur] + size_t(row) * size_t(M.ldx) + col0;
-            float x[32];
-            if (full_chunk) {
-              const uint4* src = reinterpret_cast<const uint4*>(x_row);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint4 u = src[q];
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  x[q * 8 + 2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
-                  x[q * 8 + 2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
-                }
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) x[i] = (col0 + i < n) ? bf16_bits_to_float(x_row[i]) : 0.0f;
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = fmaf(p.a, x[i], v[i]);
-            if (!LAST) {
-              uint16_t* o_row = M.X[p.cur ^ 1] + size_t(row) * size_t(M.ldx) + col0;
-              if (full_chunk) {
-                uint4* dst = reinterpret_cast<uint4*>(o_row);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  dst[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]), pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                                      pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]), pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (col0 + i < n) o_row[i] = float_to_bf16_bits(v[i]);
-              }
-            } else {
-              const float decay = p.decay;
-              const float step = p.lr * M.shape_scale;
-              if (!M.tall) {
-                // W is [m, n]: element (row, col)
-                float* w_row = M.W + size_t(row) * size_t(M.C) + col0;
-                if (full_chunk && M.vec_ok) {
-                  float4* wp = reinterpret_cast<float4*>(w_row);
-#pragma unroll
-                  for (int q = 0; q < 8; ++q) {
-                    float4 w4 = wp[q];
-                    w4.x = w4.x * decay - step * v[4 * q + 0];
-                    w4.y = w4.y * decay - step * v[4 * q + 1];
-                    w4.z = w4.z * decay - step * v[4 * q + 2];
-                    w4.w = w4.w * decay - step * v[4 * q + 3];
-                    wp[q] = w4;
-                  }
-                } else {
-#pragma unroll
-                  for (int i = 0; i < 32; ++i)
-                    if (col0 + i < n) w_row[i] = w_row[i] * decay - step * v[i];
-                }
-              } else {
-                // W is [n, m]: element (col, row); lanes hold consecutive rows
-                float* w_col = M.W + size_t(col0) * size_t(M.C) + row;
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (col0 + i < n) {
-                    float* w = w_col + size_t(i) * size_t(M.C);
-                    *w = *w * decay - step * v[i];
-                  }
-              }
-            }
-          }
-        }
-      }
+      const int cbase = int(tr.tn) * kBN + half * kEpiCols;
+      const uint32_t tb = tmem_base + uint32_t(acc) * uint32_t(kBN) + uint32_t(half * kEpiCols) +
+                          (uint32_t(quarter * 32) << 16);
+      if (PHASE == MO_PHASE_UPDATE)
+        epilogue_update<LAST>(p, M, row, cbase, tb);
+      else
+        epilogue_symmetric<PHASE>(p, M, row, cbase, tb);
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty_bar(acc));
       acc ^= 1;

@@ -76,8 +76,8 @@ class Workload:
         return sum(self.tail)
 
 
-def _gpt2l() -> Tuple[Tuple[MatrixSpec, ...], Tuple[int, ...]]:
-    h, layers = 1280, 36
+def _gpt2l(layers: int = 36) -> Tuple[Tuple[MatrixSpec, ...], Tuple[int, ...]]:
+    h = 1280
     per_layer = [MatrixSpec(3 * h, h, "qkv"), MatrixSpec(h, h, "attn_proj"),
                  MatrixSpec(4 * h, h, "fc"), MatrixSpec(h, 4 * h, "fc_proj")]
     mats = tuple(per_layer * layers)
@@ -123,6 +123,12 @@ def get_workload(name: str) -> Workload:
     if name == "gpt2l":
         m, t = _gpt2l()
         return Workload("gpt2l", 1, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
+    if name == "gpt2l_4layers":
+        # four layers of the GPT-2 Large set: the same kernels on a ~2 GB
+        # working set (each bf16 iterate buffer, 157 MB, still exceeds L2);
+        # used for profiler captures
+        m, t = _gpt2l(4)
+        return Workload("gpt2l_4layers", 5, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
     if name == "llama8b":
         m, t = _llama8b()
         return Workload("llama8b", 2, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
