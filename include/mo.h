@@ -48,7 +48,8 @@ enum mo_status {
   MO_ERR_OVERLAP = -6,           /* W, V (or p, m, v) of one entry overlap */
   MO_ERR_CUDA = -7,              /* a CUDA runtime call failed; see mo_last_cuda_error() */
   MO_ERR_DEVICE_TIMEOUT = -8,    /* a bounded device-side wait expired (see mo_last_device_error) */
-  MO_ERR_UNSUPPORTED_DEVICE = -9 /* the current device is not sm_103 */
+  MO_ERR_UNSUPPORTED_DEVICE = -9, /* the current device is not sm_103 */
+  MO_ERR_SCRATCH_LIMIT = -10      /* muon_owner_step_noalloc: table too large for the built-in scratch */
 };
 
 /* One 2D matrix of an owner's shape table ("MatrixFSDP", section 4.1: one
@@ -126,6 +127,28 @@ int muon_owner_step(const mo_matrix* tbl, int32_t n, const mo_muon_params* param
 int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params* params,
                           void* ws, size_t ws_bytes, cudaStream_t stream,
                           cudaEvent_t ev_ns_begin, cudaEvent_t ev_ns_end);
+
+/* The same Muon step for callers that cannot allocate device memory (no
+ * counterpart on the pages; it exists for the library's users). Processes
+ * whose device memory is owned by another allocator, and contexts where
+ * cudaMalloc is not allowed, cannot provide the `ws` buffer muon_owner_step
+ * needs. This entry point allocates nothing: its scratch is a file-scope
+ * device array of mo_static_scratch_bytes() bytes (64 MiB), which every device
+ * that runs this code holds until the process exits.
+ *  - Tables whose mo_muon_workspace_bytes() exceeds that size are rejected
+ *    with MO_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    each call rewrites everything the step needs zeroed. Calls that overlap
+ *    on the GPU (different streams, or concurrent host threads) race on it.
+ * Arguments, layout, results and the other status codes are those of
+ * muon_owner_step. */
+int muon_owner_step_noalloc(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, cudaStream_t stream);
+
+/* Size in bytes of the scratch array muon_owner_step_noalloc uses. */
+size_t mo_static_scratch_bytes(void);
 
 /* AdamW over every tail segment, on `stream` (one grouped launch per 256
  * segments). */

@@ -20,7 +20,7 @@ __all__ = [
     "mo_muon_workspace_bytes", "muon_workspace", "muon_owner_step", "muon_owner_step_timed",
     "rmnp_step", "rmnp_step_scaled", "adamw_tail_step", "mo_last_device_error",
     "mo_status_string", "mo_selftest_bounded_wait", "mo_muon_tile_schedule", "MuonTable",
-    "TailTable", "RmnpTable",
+    "TailTable", "RmnpTable", "muon_owner_step_noalloc", "mo_static_scratch_bytes",
 ]
 
 MO_OK = 0
@@ -101,6 +101,8 @@ def load_library() -> ctypes.CDLL:
         "mo_abi_version": (ctypes.c_int, []),
         "mo_muon_tile_schedule": (ctypes.c_int, [P, I32, I32, P, I64, P]),
         "mo_selftest_bounded_wait": (ctypes.c_int, [I64, P]),
+        "muon_owner_step_noalloc": (ctypes.c_int, [P, I32, P, P]),
+        "mo_static_scratch_bytes": (SZ, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -215,6 +217,21 @@ def muon_owner_step_timed(mats, params, workspace, ev_begin, ev_end, stream=None
         _stream_ptr(stream), ev_begin.cuda_event if ev_begin is not None else None,
         ev_end.cuda_event if ev_end is not None else None)
     _check(st, "muon_owner_step_timed")
+
+
+def muon_owner_step_noalloc(mats, params: Optional[MuonParams] = None, stream=None) -> None:
+    """muon_owner_step without a caller workspace, for callers that cannot
+    allocate device memory: the library's fixed scratch array is used instead
+    (tables up to mo_static_scratch_bytes() of workspace). Calls that overlap
+    on the GPU share that array and race."""
+    t = _as_table(mats)
+    params = params or MuonParams()
+    _check(load_library().muon_owner_step_noalloc(t.ptr, t.n, ctypes.byref(params), _stream_ptr(stream)),
+           "muon_owner_step_noalloc")
+
+
+def mo_static_scratch_bytes() -> int:
+    return int(load_library().mo_static_scratch_bytes())
 
 
 # ---------------------------------------------------------------- RMNP / AdamW

@@ -194,6 +194,10 @@ int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmn
 
 }  // namespace
 
+namespace mo {
+void note_cuda_error(int e) { t_last_cuda_error = e; }
+}  // namespace mo
+
 extern "C" {
 
 size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_params* params) {
@@ -294,6 +298,7 @@ const char* mo_status_string(int status) {
     case MO_ERR_CUDA: return "CUDA runtime error";
     case MO_ERR_DEVICE_TIMEOUT: return "bounded device-side wait expired";
     case MO_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103";
+    case MO_ERR_SCRATCH_LIMIT: return "table needs more scratch than the built-in array holds (mo_static_scratch_bytes)";
     default: return "unknown status";
   }
 }
