@@ -188,7 +188,7 @@ int mo_abi_version(void);
 /* One output tile of a grouped Newton-Schulz GEMM launch. */
 typedef struct {
   uint32_t mat;   /* index into the shape table */
-  uint16_t tm;    /* tile row (units of 128 rows) */
+  uint16_t tm;    /* tile row (units of 256 rows: one CTA pair) */
   uint16_t tn;    /* tile column (units of 256 columns) */
 } mo_tile;
 

@@ -426,6 +426,229 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+//
+// Same three products with 256 x 256 output tiles computed by a cluster of
+// two CTAs on two SMs (tcgen05 cta_group::2). Each CTA stages its 128-row half
+// of the A operand and its 128-row (or 128-column) half of the B operand, so
+// a 256 x 256 tile streams 64 KB per K block instead of the 96 KB two
+// independent 128 x 256 tiles would need. The even CTA issues the MMAs and
+// multicasts their completion to both CTAs; each CTA's epilogue drains the
+// accumulator rows of its own A half from its own TMEM.
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairHalfBytes = 128 * kBK * 2;                  // 16 KB
+constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;            // A half + B half
+constexpr uint32_t kPairNumBars = 2 * kPairStages + 5;
+constexpr size_t kPairSmem = 1024 + size_t(kPairStages) * kPairStageBytes + 8 * kPairNumBars + 16;
+
+template <int PHASE, bool LAST>
+__global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_constant__ NsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + uint32_t(kPairStages) * kPairStageBytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + size_t(kPairStages) * kPairStageBytes + 8 * kPairNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto full_bar = [&](int s) { return bars + 8u * uint32_t(s); };
+  auto empty_bar = [&](int s) { return bars + 8u * uint32_t(kPairStages + s); };
+  auto tfull_bar = [&](int s) { return bars + 8u * uint32_t(2 * kPairStages + s); };
+  auto tempty_bar = [&](int s) { return bars + 8u * uint32_t(2 * kPairStages + 2 + s); };
+  const uint32_t drain_bar = bars + 8u * uint32_t(2 * kPairStages + 4);
+
+  const int warp = int(threadIdx.x >> 5);
+  const int lane = int(threadIdx.x & 31);
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cid = int(ptx::cluster_id_x());
+  const int ncl = int(ptx::nclusters_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(tfull_bar(s), 1);
+      ptx::mbar_init(tempty_bar(s), 2 * kEpiWarps);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer (both CTAs)
+      int32_t pending[kPairStages];
+      for (int s = 0; s < kPairStages; ++s) pending[s] = -1;
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      uint32_t last_mat = 0xFFFFFFFFu;
+      for (int t = cid; ok && t < p.ntiles; t += ncl) {
+        const TileRec tr = p.tiles[t];
+        const DevMat& M = p.mats[tr.mat];
+        const CUtensorMap* maps = p.tmaps + size_t(tr.mat) * kMapsPerMat;
+        const void* mapA;
+        const void* mapB;
+        int K;
+        if (PHASE == MO_PHASE_GRAM) {
+          mapA = mapB = &maps[p.cur];
+          K = M.n;
+        } else if (PHASE == MO_PHASE_POLY) {
+          mapA = mapB = &maps[2];
+          K = M.m;
+        } else {
+          mapA = &maps[3];
+          mapB = &maps[p.cur];
+          K = M.m;
+        }
+        if (tr.mat != last_mat) {
+          ptx::fence_tmap_acquire(mapA);
+          ptx::fence_tmap_acquire(mapB);
+          last_mat = tr.mat;
+        }
+        const int nk = (K + kBK - 1) / kBK;
+        const int arow = int(tr.tm) * 256 + int(rank) * 128;   // this CTA's A rows
+        const int bcol = int(tr.tn) * 256 + int(rank) * 128;   // this CTA's B rows / columns
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb_local = full_bar(stage);
+          if (leader) ptx::mbar_arrive_expect_tx(fb_local, 2 * kPairStageBytes);
+          const uint32_t fb = ptx::mapa_shared(fb_local, 0);
+          const uint32_t sa = base + uint32_t(stage) * kPairStageBytes;
+          const uint32_t sb = sa + kPairHalfBytes;
+          const int k0 = kb * kBK;
+          ptx::tma_load_2d_pair(sa, mapA, fb, k0, arow);
+          ptx::tma_load_2d_pair(sa + kBoxBytes, mapA, fb, k0, arow + 64);
+          if (PHASE != MO_PHASE_UPDATE) {
+            ptx::tma_load_2d_pair(sb, mapB, fb, k0, bcol);
+            ptx::tma_load_2d_pair(sb + kBoxBytes, mapB, fb, k0, bcol + 64);
+          } else {
+            ptx::tma_load_2d_pair(sb, mapB, fb, bcol, k0);
+            ptx::tma_load_2d_pair(sb + kBoxBytes, mapB, fb, bcol + 64, k0);
+          }
+          pending[stage] = int32_t(ph);
+          if (++stage == kPairStages) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        if (leader) {
+          // the leader's full barriers count both CTAs' bytes
+          for (int s = 0; s < kPairStages; ++s)
+            if (pending[s] >= 0) mbar_wait_drain(full_bar(s), uint32_t(pending[s]), p.timeout_ns);
+        } else {
+          // the peer cannot observe the leader's barriers: give its copies time to land
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (ptx::globaltimer_ns() - t0 < 2000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issuer (even CTA)
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, kBN, 0u, PHASE == MO_PHASE_UPDATE ? 1u : 0u);
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      bool issued = false;
+      bool ok = true;
+      for (int t = cid; ok && t < p.ntiles; t += ncl) {
+        const TileRec tr = p.tiles[t];
+        const DevMat& M = p.mats[tr.mat];
+        const int K = (PHASE == MO_PHASE_GRAM) ? M.n : M.m;
+        const int nk = (K + kBK - 1) / kBK;
+        if (!mbar_wait_bounded(tempty_bar(acc), aph ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(acc) * uint32_t(kBN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), ph, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = base + uint32_t(stage) * kPairStageBytes;
+          const uint32_t sb = sa + kPairHalfBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(sa + uint32_t(kk) * 32u, 16u, 1024u);
+            const uint64_t bd = (PHASE == MO_PHASE_UPDATE)
+                                    ? ptx::smem_desc_sw128(sb + uint32_t(kk) * 2048u, kBoxBytes, 1024u)
+                                    : ptx::smem_desc_sw128(sb + uint32_t(kk) * 32u, 16u, 1024u);
+            ptx::umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit_pair(empty_bar(stage), 0x3);
+          issued = true;
+          if (++stage == kPairStages) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::umma_commit_pair(tfull_bar(acc), 0x3);
+        acc ^= 1;
+        if (acc == 0) aph ^= 1u;
+      }
+      if (*abort_flag && issued) {
+        ptx::umma_commit_pair(drain_bar, 0x1);
+        mbar_wait_drain(drain_bar, 0u, p.timeout_ns);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int r_in = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = cid; t < p.ntiles; t += ncl) {
+      const TileRec tr = p.tiles[t];
+      const DevMat& M = p.mats[tr.mat];
+      bool ok = mbar_wait_bounded(tfull_bar(acc), aph, abort_flag, p.status, p.timeout_ns);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int row = int(tr.tm) * 256 + int(rank) * 128 + r_in;
+      const int cbase = int(tr.tn) * kBN + half * kEpiCols;
+      const uint32_t tb = tmem_base + uint32_t(acc) * uint32_t(kBN) + uint32_t(half * kEpiCols) +
+                          (uint32_t(quarter * 32) << 16);
+      if (PHASE == MO_PHASE_UPDATE)
+        epilogue_update<LAST>(p, M, row, cbase, tb);
+      else
+        epilogue_symmetric<PHASE>(p, M, row, cbase, tb);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
 // Single-CTA kernel that waits on a barrier nothing completes; exercises the
 // bounded-wait path.
 __global__ void bounded_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
@@ -444,6 +667,28 @@ __global__ void bounded_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 }
 
 template <int PHASE, bool LAST>
+cudaError_t launch_pair(const NsParams& p, int grid, cudaStream_t stream) {
+  auto kern = ns_gemm_pair_kernel<PHASE, LAST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kPairSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int PHASE, bool LAST>
 cudaError_t launch_one(const NsParams& p, int grid, cudaStream_t stream) {
   auto kern = ns_gemm_kernel<PHASE, LAST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemmSmem));
@@ -455,6 +700,19 @@ cudaError_t launch_one(const NsParams& p, int grid, cudaStream_t stream) {
 }  // namespace
 
 size_t ns_gemm_smem_bytes() { return kGemmSmem; }
+
+cudaError_t launch_ns_phase_pair(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream) {
+  if (p.ntiles <= 0) return cudaSuccess;
+  switch (phase) {
+    case MO_PHASE_GRAM:
+      return launch_pair<MO_PHASE_GRAM, false>(p, grid, stream);
+    case MO_PHASE_POLY:
+      return launch_pair<MO_PHASE_POLY, false>(p, grid, stream);
+    default:
+      return last ? launch_pair<MO_PHASE_UPDATE, true>(p, grid, stream)
+                  : launch_pair<MO_PHASE_UPDATE, false>(p, grid, stream);
+  }
+}
 
 cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream) {
   if (p.ntiles <= 0) return cudaSuccess;

@@ -108,7 +108,7 @@ int validate_adamw(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* p)
   return MO_OK;
 }
 
-void build_tiles(const mo_matrix* tbl, int32_t n, int phase, std::vector<TileRec>& out) {
+void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector<TileRec>& out) {
   struct Key {
     int64_t k;
     TileRec t;
@@ -117,7 +117,7 @@ void build_tiles(const mo_matrix* tbl, int32_t n, int phase, std::vector<TileRec
   for (int32_t i = 0; i < n; ++i) {
     const int64_t R = tbl[i].rows, C = tbl[i].cols;
     const int64_t m = std::min(R, C), nn = std::max(R, C);
-    const int64_t tiles_m = ceil_div(m, kBM);
+    const int64_t tiles_m = ceil_div(m, bm);
     if (phase == MO_PHASE_UPDATE) {
       const int64_t tiles_n = ceil_div(nn, kBN);
       for (int64_t tm = 0; tm < tiles_m; ++tm)
@@ -130,7 +130,7 @@ void build_tiles(const mo_matrix* tbl, int32_t n, int phase, std::vector<TileRec
       const int64_t k = (phase == MO_PHASE_GRAM) ? nn : m;
       for (int64_t tm = 0; tm < tiles_m; ++tm)
         for (int64_t tn = 0; tn < tiles_n; ++tn)
-          if ((tn + 1) * kBN > tm * kBM) keys.push_back({k, {uint32_t(i), uint16_t(tm), uint16_t(tn)}});
+          if ((tn + 1) * kBN > tm * bm) keys.push_back({k, {uint32_t(i), uint16_t(tm), uint16_t(tn)}});
     }
   }
   std::sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
@@ -143,7 +143,7 @@ void build_tiles(const mo_matrix* tbl, int32_t n, int phase, std::vector<TileRec
   for (size_t j = 0; j < keys.size(); ++j) out[j] = keys[j].t;
 }
 
-void plan_muon(const mo_matrix* tbl, int32_t n, MuonLayout& L) {
+void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L) {
   L.n = n;
   L.mats.assign(size_t(n), DevMat{});
   L.nrm_prefix.assign(size_t(n) + 1, 0);
@@ -176,7 +176,7 @@ void plan_muon(const mo_matrix* tbl, int32_t n, MuonLayout& L) {
   L.cast_prefix[size_t(n)] = cast;
   L.nrm_total = nrm;
   L.cast_total = cast;
-  for (int ph = 0; ph < 3; ++ph) build_tiles(tbl, n, ph, L.tiles[ph]);
+  for (int ph = 0; ph < 3; ++ph) build_tiles(tbl, n, ph, bm, L.tiles[ph]);
 
   size_t off = 0;
   L.off_meta = off;

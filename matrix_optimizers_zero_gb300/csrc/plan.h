@@ -34,10 +34,11 @@ int validate_muon_params(const mo_muon_params* p);
 int validate_rmnp_params(const mo_rmnp_params* p);
 int validate_adamw(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* p);
 
-// Tile schedule of one phase (MO_PHASE_*), sorted into launch order.
-void build_tiles(const mo_matrix* tbl, int32_t n, int phase, std::vector<TileRec>& out);
+// Tile schedule of one phase (MO_PHASE_*), sorted into launch order; bm is
+// the output tile height (128 rows for one CTA, 256 for a CTA pair).
+void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector<TileRec>& out);
 
 // Layout of the Muon workspace for a validated table.
-void plan_muon(const mo_matrix* tbl, int32_t n, MuonLayout& L);
+void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L);
 
 }  // namespace mo

@@ -48,11 +48,14 @@ def test_status_strings(lib):
 
 # ---------------------------------------------------------------- schedules
 
+BM = 256   # output tile height of the CTA-pair kernel
+
+
 def py_schedule(shapes, phase):
     keys = []
     for i, (R, C) in enumerate(shapes):
         m, n = min(R, C), max(R, C)
-        tiles_m = -(-m // 128)
+        tiles_m = -(-m // BM)
         if phase == mo.PHASE_UPDATE:
             for tm in range(tiles_m):
                 for tn in range(-(-n // 256)):
@@ -61,7 +64,7 @@ def py_schedule(shapes, phase):
             k = n if phase == mo.PHASE_GRAM else m
             for tm in range(tiles_m):
                 for tn in range(-(-m // 256)):
-                    if (tn + 1) * 256 > tm * 128:
+                    if (tn + 1) * 256 > tm * BM:
                         keys.append((-k, i, tm, tn))
     keys.sort()
     return [(i, tm, tn) for _, i, tm, tn in keys]
@@ -87,9 +90,9 @@ def test_schedule_covers_outputs_exactly_once(lib, shape):
     for phase in (0, 1):
         cover = np.zeros((m, m), dtype=np.int32)
         for _, tm, tn in mo.mo_muon_tile_schedule([shape], phase):
-            r0, c0 = tm * 128, tn * 256
+            r0, c0 = tm * BM, tn * 256
             # the epilogue's store rule: direct for col >= row, mirror for col > row
-            for r in range(r0, min(r0 + 128, m)):
+            for r in range(r0, min(r0 + BM, m)):
                 for c in range(c0, min(c0 + 256, m)):
                     if c >= r:
                         cover[r, c] += 1
@@ -98,7 +101,7 @@ def test_schedule_covers_outputs_exactly_once(lib, shape):
         assert np.all(cover == 1), phase
     cover = np.zeros((m, n), dtype=np.int32)
     for _, tm, tn in mo.mo_muon_tile_schedule([shape], 2):
-        cover[tm * 128:tm * 128 + 128, tn * 256:tn * 256 + 256] += 1
+        cover[tm * BM:tm * BM + BM, tn * 256:tn * 256 + 256] += 1
     assert np.all(cover == 1)
 
 
