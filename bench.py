@@ -45,6 +45,27 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# ---------------------------------------------------------------- multi-rank helpers
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of x over all ranks of the default process group (x itself
+    when there is none). NCCL groups reduce on `device`, others on the CPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    on = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=on)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, ms_max: float) -> float:
+    """Aggregate throughput of `world` independent replicas that each did
+    flops_per_rank of work, timed by the slowest rank."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -278,12 +299,8 @@ def run_ours(args, rank, world, local_rank):
     adam_gbs = wl.tail_elements * workloads.ADAMW_BYTES_PER_EL / (adam_ms * 1e-3) / 1e9
     pro_gbs = n_el * 16 / (pro_ms * 1e-3) / 1e9
 
-    # max over ranks
-    t_rank = torch.tensor([ms_step], device=dev, dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(t_rank, op=dist.ReduceOp.MAX)
-    ms_max = float(t_rank.item())
-    value = world * ns_flops / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms_step, dev)
+    value = whole_job_tflops(world, ns_flops, ms_max)
 
     # ---- end to end through the C ABI with host buffers
     e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 10))
@@ -311,11 +328,8 @@ def run_ours(args, rank, world, local_rank):
         hP.copy_(Pf, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / max(e2e_steps, 1)
-    t_e2e = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
-    e2e_value = world * ns_flops / (float(t_e2e.item()) * 1e-3) / 1e12
+    e2e_ms_max = max_over_ranks(e0.elapsed_time(e1) / max(e2e_steps, 1), dev)
+    e2e_value = whole_job_tflops(world, ns_flops, e2e_ms_max)
     if mo.mo_last_device_error() != 0:
         raise RuntimeError("device-side timeout during the timed region")
 
@@ -370,7 +384,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
         },
         "e2e": ({"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(float(t_e2e.item()), 3)}
+                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms_max, 3)}
                 if e2e_steps else None),
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk,

@@ -211,6 +211,7 @@ def host_matrix(wl: Workload, index: int, seed: int = BASE_SEED, v_std: float = 
         v = _rng(wl.config_id, index, _ROLE_V, seed).standard_normal(shape, dtype=np.float32) * np.float32(v_std)
     else:
         v = np.zeros(shape, dtype=np.float32)
+    w, g32, v = (np.ascontiguousarray(x) for x in (w, g32, v))
     return (torch.from_numpy(w), torch.from_numpy(g32).to(torch.bfloat16), torch.from_numpy(v))
 
 

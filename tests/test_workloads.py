@@ -86,6 +86,8 @@ def test_structured_spectrum_generation():
         assert s.min() >= 1e-4 and s.max() <= 1.0
         G = wl_mod.exact_matrix(small, i)
         np.testing.assert_allclose(np.linalg.svd(G, compute_uv=False), np.sort(s)[::-1], rtol=1e-10)
+    for i in range(3):
+        assert all(t.is_contiguous() for t in wl_mod.host_matrix(small, i))
     G = wl_mod.exact_matrix(small, 2)
     gram = G @ G.T
     np.testing.assert_allclose(gram - np.diag(np.diag(gram)), 0, atol=1e-12)
