@@ -20,15 +20,6 @@ namespace {
 
 thread_local int t_last_cuda_error = 0;
 
-// Output tile height of the Newton-Schulz GEMMs: 256 rows on CTA pairs
-// (the default), 128 rows on single CTAs when MO_NS_SINGLE_CTA=1.
-int ns_tile_m() {
-  static const int bm = [] {
-    const char* e = std::getenv("MO_NS_SINGLE_CTA");
-    return (e && std::atoi(e) != 0) ? 128 : 256;
-  }();
-  return bm;
-}
 
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = int(e);
@@ -85,7 +76,7 @@ int muon_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* 
   if (!ws) return MO_ERR_NULL_POINTER;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MO_ERR_MISALIGNED;
   mo::MuonLayout L;
-  mo::plan_muon(tbl, n, ns_tile_m(), L);
+  mo::plan_muon(tbl, n, mo::kBM, L);
   if (ws_bytes < L.total_bytes) return MO_ERR_WORKSPACE_TOO_SMALL;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MO_OK) return st;
@@ -151,13 +142,8 @@ int muon_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* 
       np.tiles = reinterpret_cast<const mo::TileRec*>(wsb + L.off_tiles[ph]);
       np.ntiles = int32_t(L.tiles[ph].size());
       const bool last = (ph == MO_PHASE_UPDATE) && (it == prm->ns_steps - 1);
-      if (ns_tile_m() == 256) {
-        const int grid = 2 * std::max(1, std::min(np.ntiles, dev->sms / 2));
-        if ((e = mo::launch_ns_phase_pair(ph, last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
-      } else {
-        const int grid = std::max(1, std::min(np.ntiles, dev->sms));
-        if ((e = mo::launch_ns_phase(ph, last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
-      }
+      const int grid = 2 * std::max(1, std::min(np.ntiles, dev->sms / 2));
+      if ((e = mo::launch_ns_phase(ph, last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
     }
     cur ^= 1;
   }
@@ -221,7 +207,7 @@ size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_pa
   if (mo::validate_matrix_table(tbl, n) != MO_OK) return 0;
   if (n == 0) return 0;
   mo::MuonLayout L;
-  mo::plan_muon(tbl, n, ns_tile_m(), L);
+  mo::plan_muon(tbl, n, mo::kBM, L);
   return L.total_bytes;
 }
 
@@ -328,7 +314,7 @@ int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase, mo_til
   int st = mo::validate_matrix_table(tbl, n);
   if (st != MO_OK) return st;
   std::vector<mo::TileRec> tiles;
-  mo::build_tiles(tbl, n, phase, ns_tile_m(), tiles);
+  mo::build_tiles(tbl, n, phase, mo::kBM, tiles);
   *count = int64_t(tiles.size());
   if (cap < int64_t(tiles.size())) return MO_ERR_BAD_SHAPE;
   if (!tiles.empty()) {

@@ -24,9 +24,8 @@ struct NsParams {
   uint64_t timeout_ns;
 };
 
-cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream);
 // 256 x 256 tiles on CTA pairs; grid must be even (two CTAs per cluster)
-cudaError_t launch_ns_phase_pair(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream);
 size_t ns_gemm_smem_bytes();
 bool encode_matrix_maps(const DevMat& d, void* out_maps);   // writes kMapsPerMat CUtensorMap
 cudaError_t device_status_ptr(int** out);

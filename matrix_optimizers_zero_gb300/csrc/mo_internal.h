@@ -9,9 +9,10 @@
 
 namespace mo {
 
-// Newton-Schulz GEMM tiling: one UMMA M=128 x N=256 accumulator per tile,
-// 64-element (128-byte, one swizzle row) K blocks.
-constexpr int kBM = 128;
+// Newton-Schulz GEMM tiling: 256 x 256 output tiles computed by a pair of
+// CTAs (UMMA M=256 across the pair, N=256), 64-element (128-byte, one
+// swizzle row) K blocks.
+constexpr int kBM = 256;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 

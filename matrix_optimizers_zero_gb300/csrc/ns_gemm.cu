@@ -10,13 +10,17 @@
 //                                    W <- W (1 - lr wd) - lr s X' instead)
 // X0 = bf16(V / (||V||_F + eps)) is written by the prologue.
 //
-// Kernel structure (one persistent CTA per SM, 10 warps):
-//   warp 0      TMA producer: 128x64 A-operand and 256x64 B-operand boxes
-//               (128-byte swizzle) into a 4-stage shared-memory ring
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//               (M=128, N=256, K=16 per instruction, fp32 accumulate)
-//   warps 2-9   epilogue: tcgen05.ld of the accumulator (one TMEM lane and
-//               128 columns per thread), fused arithmetic, bf16/fp32 stores
+// Kernel structure: persistent clusters of two CTAs on two SMs (tcgen05
+// cta_group::2), 256 x 256 output tiles, 10 warps per CTA:
+//   warp 0      TMA producer: this CTA's 128-row halves of the A and B
+//               operands in 64 x 64 boxes (128-byte swizzle) into a 6-stage
+//               shared-memory ring; completion counted on the even CTA's
+//               barriers
+//   warp 1      TMEM allocation (both CTAs); the even CTA's lane 0 issues
+//               tcgen05.mma (M=256, N=256, K=16, fp32 accumulate) and
+//               multicasts the completion commits to both CTAs
+//   warps 2-9   epilogue: tcgen05.ld of this CTA's accumulator rows (one TMEM
+//               lane and 128 columns per thread), fused arithmetic, stores
 // The two 256-column accumulators in TMEM let the epilogue of one tile run
 // under the main loop of the next.
 #include <cuda.h>
@@ -37,60 +41,58 @@ __device__ int g_mo_status = 0;
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;                 // one TMA box: 64 x 64 bf16
-constexpr uint32_t kTileABytes = kBM * kBK * 2;             // 16 KB
-constexpr uint32_t kTileBBytes = kBN * kBK * 2;             // 32 KB
-constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes; // 48 KB
 constexpr int kEpiWarps = 8;                                 // two per TMEM lane quarter
 constexpr int kEpiCols = kBN / 2;                            // accumulator columns per epilogue thread
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;                         // 2 accumulators x 256 fp32 columns
-constexpr uint32_t kNumBars = 2 * kStages + 5;              // full, empty, tfull x2, tempty x2, drain
-constexpr size_t kGemmSmem = 1024 + size_t(kStages) * kStageBytes + 8 * kNumBars + 16;
-
-static_assert(kBM == 128 && kBN == 256 && kBK == 64, "tile shape baked into the descriptors");
+static_assert(kBM == 256 && kBN == 256 && kBK == 64, "tile shape baked into the descriptors");
 
 // ------------------------------------------------------------------ epilogues
 // Each epilogue thread owns one accumulator row (TMEM lane) and kEpiCols
 // consecutive columns of it, processed in chunks of 32. Operand loads for the
 // next chunk are issued before the current chunk's accumulator is read, and
-// every load of a chunk is issued before its stores.
+// every load of a chunk is issued before its stores. Row accesses use 32-byte
+// vectors: a warp instruction then moves whole 32-byte sectors (one per row),
+// which measurably leaves more L2 bandwidth to the TMA operand stream than
+// 16-byte accesses do.
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* x) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    x[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
-    x[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
-  }
-}
-
-__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
-  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                    pack_bf16x2(v[6], v[7]));
-}
-
-// Loads the 32 bf16 values of `row_ptr[col0 .. col0+32)` as four 16-byte
+// Loads the 32 bf16 values of `row_ptr[col0 .. col0+32)` as two 32-byte
 // vectors when the whole chunk is inside the row (valid = row in range).
 __device__ __forceinline__ void prefetch_chunk(const uint16_t* row_ptr, int col0, int ncols, bool valid,
-                                               uint4 (&dst)[4]) {
+                                               uint32_t (&dst)[16]) {
   if (valid && col0 + 32 <= ncols) {
-    const uint4* src = reinterpret_cast<const uint4*>(row_ptr + col0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) dst[q] = src[q];
+    uint32_t (&lo)[8] = *reinterpret_cast<uint32_t (*)[8]>(&dst[0]);
+    uint32_t (&hi)[8] = *reinterpret_cast<uint32_t (*)[8]>(&dst[8]);
+    ptx::ld_global_v8(row_ptr + col0, lo);
+    ptx::ld_global_v8(row_ptr + col0 + 16, hi);
   }
 }
 
 __device__ __forceinline__ void chunk_operand(const uint16_t* row_ptr, int col0, int ncols,
-                                              const uint4 (&pre)[4], float (&x)[32]) {
+                                              const uint32_t (&pre)[16], float (&x)[32]) {
   if (col0 + 32 <= ncols) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) unpack_bf16x8(pre[q], &x[q * 8]);
+    for (int j = 0; j < 16; ++j) {
+      x[2 * j] = bf16_bits_to_float(pre[j] & 0xFFFFu);
+      x[2 * j + 1] = bf16_bits_to_float(pre[j] >> 16);
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = (col0 + i < ncols) ? bf16_bits_to_float(row_ptr[col0 + i]) : 0.0f;
   }
+}
+
+// Stores 32 values as bf16 with two 32-byte vectors.
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
+  uint32_t lo[8], hi[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    lo[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    hi[j] = pack_bf16x2(v[16 + 2 * j], v[16 + 2 * j + 1]);
+  }
+  ptx::st_global_v8(dst, lo);
+  ptx::st_global_v8(dst + 16, hi);
 }
 
 __device__ __forceinline__ void tmem_chunk(uint32_t taddr, float (&v)[32]) {
@@ -102,9 +104,32 @@ __device__ __forceinline__ void tmem_chunk(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Pulls the W elements the last update's epilogue will read for this
+// thread's row and 128 columns into L2 while the main loop still runs.
+__device__ __forceinline__ void prefetch_w_rows(const DevMat& M, int row, int cbase) {
+  const int lane = int(threadIdx.x & 31);
+  if (row >= M.m || cbase >= M.n) return;
+  if (!M.tall) {
+    const float* w = M.W + size_t(row) * size_t(M.C) + cbase;
+    const int cols = min(kEpiCols, M.n - cbase);
+    for (int c = 0; c < cols; c += 32) ptx::prefetch_l2(w + c);
+  } else {
+    // W is [n, m]: the warp's 32 rows are one 128-byte line per column
+    const int row_base = row - lane;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int col = cbase + lane * 4 + q;
+      if (col < M.n) ptx::prefetch_l2(M.W + size_t(col) * size_t(M.C) + row_base);
+    }
+  }
+}
+
 // GRAM: A = acc.  POLY: B = b A + c acc.  Stored bf16 to the upper triangle
 // (col >= row) and mirrored to the strict lower triangle, so every element of
-// the symmetric result is written exactly once.
+// the symmetric result is written exactly once. The mirrored stores are one
+// element per lane; across a warp (32 consecutive rows) each is one
+// contiguous 64-byte segment. (Staging the mirror through shared memory was
+// measured slower: the main loop needs the shared-memory bandwidth.)
 template <int PHASE>
 __device__ __forceinline__ void epilogue_symmetric(const NsParams& p, const DevMat& M, int row, int cbase,
                                                    uint32_t tb) {
@@ -113,14 +138,14 @@ __device__ __forceinline__ void epilogue_symmetric(const NsParams& p, const DevM
   const bool rv = row < m;
   uint16_t* out = (PHASE == MO_PHASE_GRAM) ? M.A : M.B;
   const uint16_t* a_row = M.A + size_t(rv ? row : 0) * ld;
-  uint4 pre[4], nxt[4];
+  uint32_t pre[16], nxt[16];
   if (PHASE == MO_PHASE_POLY) prefetch_chunk(a_row, cbase, m, rv, nxt);
 #pragma unroll 1
   for (int ch = 0; ch < kEpiCols / 32; ++ch) {
     const int col0 = cbase + ch * 32;
     if (PHASE == MO_PHASE_POLY) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) pre[q] = nxt[q];
+      for (int q = 0; q < 16; ++q) pre[q] = nxt[q];
       if (ch + 1 < kEpiCols / 32) prefetch_chunk(a_row, col0 + 32, m, rv, nxt);
     }
     float v[32];
@@ -134,9 +159,7 @@ __device__ __forceinline__ void epilogue_symmetric(const NsParams& p, const DevM
     }
     uint16_t* o_row = out + size_t(row) * ld + col0;
     if (col0 + 32 <= m && col0 >= row) {
-      uint4* dst = reinterpret_cast<uint4*>(o_row);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = pack_bf16x8(&v[q * 8]);
+      store_bf16x32(o_row, v);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -158,13 +181,13 @@ __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat&
   const int m = M.m, n = M.n;
   const bool rv = row < m;
   const uint16_t* x_row = M.X[p.cur] + size_t(rv ? row : 0) * size_t(M.ldx);
-  uint4 pre[4], nxt[4];
+  uint32_t pre[16], nxt[16];
   prefetch_chunk(x_row, cbase, n, rv, nxt);
 #pragma unroll 1
   for (int ch = 0; ch < kEpiCols / 32; ++ch) {
     const int col0 = cbase + ch * 32;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) pre[q] = nxt[q];
+    for (int q = 0; q < 16; ++q) pre[q] = nxt[q];
     if (ch + 1 < kEpiCols / 32) prefetch_chunk(x_row, col0 + 32, n, rv, nxt);
     float v[32];
     tmem_chunk(tb + uint32_t(ch * 32), v);
@@ -179,9 +202,7 @@ __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat&
     if (!LAST) {
       uint16_t* o_row = M.X[p.cur ^ 1] + size_t(row) * size_t(M.ldx) + col0;
       if (full) {
-        uint4* dst = reinterpret_cast<uint4*>(o_row);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = pack_bf16x8(&v[q * 8]);
+        store_bf16x32(o_row, v);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
@@ -193,20 +214,17 @@ __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat&
       if (!M.tall) {
         // W is [m, n]: element (row, col)
         float* w_row = M.W + size_t(row) * size_t(M.C) + col0;
-        if (full && M.vec_ok) {
-          float4* wp = reinterpret_cast<float4*>(w_row);
-          float4 w4[8];
+        if (full && (reinterpret_cast<uintptr_t>(w_row) & 31u) == 0) {
+          uint32_t w8[4][8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) w4[q] = wp[q];
+          for (int q = 0; q < 4; ++q) ptx::ld_global_v8(w_row + 8 * q, w8[q]);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            w4[q].x = fmaf(w4[q].x, decay, -step * v[4 * q + 0]);
-            w4[q].y = fmaf(w4[q].y, decay, -step * v[4 * q + 1]);
-            w4[q].z = fmaf(w4[q].z, decay, -step * v[4 * q + 2]);
-            w4[q].w = fmaf(w4[q].w, decay, -step * v[4 * q + 3]);
-          }
+          for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int q = 0; q < 8; ++q) wp[q] = w4[q];
+            for (int j = 0; j < 8; ++j)
+              w8[q][j] = __float_as_uint(fmaf(__uint_as_float(w8[q][j]), decay, -step * v[8 * q + j]));
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ptx::st_global_v8(w_row + 8 * q, w8[q]);
         } else {
           float w[32];
 #pragma unroll
@@ -230,202 +248,6 @@ __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat&
   }
 }
 
-template <int PHASE, bool LAST>
-__global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ NsParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = ptx::smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bars = base + uint32_t(kStages) * kStageBytes;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + size_t(kStages) * kStageBytes + 8 * kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  auto full_bar = [&](int s) { return bars + 8u * uint32_t(s); };
-  auto empty_bar = [&](int s) { return bars + 8u * uint32_t(kStages + s); };
-  auto tfull_bar = [&](int s) { return bars + 8u * uint32_t(2 * kStages + s); };
-  auto tempty_bar = [&](int s) { return bars + 8u * uint32_t(2 * kStages + 2 + s); };
-  const uint32_t drain_bar = bars + 8u * uint32_t(2 * kStages + 4);
-
-  const int warp = int(threadIdx.x >> 5);
-  const int lane = int(threadIdx.x & 31);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(tfull_bar(s), 1);
-      ptx::mbar_init(tempty_bar(s), 32 * kEpiWarps);
-    }
-    ptx::mbar_init(drain_bar, 1);
-    *abort_flag = 0;
-    ptx::fence_mbar_init();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      int32_t pending[kStages];
-      for (int s = 0; s < kStages; ++s) pending[s] = -1;
-      int stage = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      uint32_t last_mat = 0xFFFFFFFFu;
-      for (int t = int(blockIdx.x); ok && t < p.ntiles; t += int(gridDim.x)) {
-        const TileRec tr = p.tiles[t];
-        const DevMat& M = p.mats[tr.mat];
-        const CUtensorMap* maps = p.tmaps + size_t(tr.mat) * kMapsPerMat;
-        const void* mapA;
-        const void* mapB;
-        int K;
-        if (PHASE == MO_PHASE_GRAM) {
-          mapA = mapB = &maps[p.cur];
-          K = M.n;
-        } else if (PHASE == MO_PHASE_POLY) {
-          mapA = mapB = &maps[2];
-          K = M.m;
-        } else {
-          mapA = &maps[3];
-          mapB = &maps[p.cur];
-          K = M.m;
-        }
-        const int nk = (K + kBK - 1) / kBK;
-        const int row0 = int(tr.tm) * kBM;
-        const int col0 = int(tr.tn) * kBN;
-        if (tr.mat != last_mat) {
-          ptx::fence_tmap_acquire(mapA);
-          ptx::fence_tmap_acquire(mapB);
-          last_mat = tr.mat;
-        }
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(empty_bar(stage), ph ^ 1u, abort_flag, p.status, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = full_bar(stage);
-          ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-          const uint32_t sa = base + uint32_t(stage) * kStageBytes;
-          const uint32_t sb = sa + kTileABytes;
-          const int k0 = kb * kBK;
-          ptx::tma_load_2d(sa, mapA, fb, k0, row0);
-          ptx::tma_load_2d(sa + kBoxBytes, mapA, fb, k0, row0 + 64);
-          if (PHASE != MO_PHASE_UPDATE) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ptx::tma_load_2d(sb + q * kBoxBytes, mapB, fb, k0, col0 + 64 * q);
-          } else {
-            // B operand X[k0:k0+64, col0:col0+256] in MN-major boxes of 64 columns
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ptx::tma_load_2d(sb + q * kBoxBytes, mapB, fb, col0 + 64 * q, k0);
-          }
-          pending[stage] = int32_t(ph);
-          if (++stage == kStages) {
-            stage = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-      if (*abort_flag) {
-        // never leave the CTA with bulk copies still landing in its shared memory
-        for (int s = 0; s < kStages; ++s)
-          if (pending[s] >= 0) mbar_wait_drain(full_bar(s), uint32_t(pending[s]), p.timeout_ns);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc =
-          ptx::idesc_bf16_f32(kBM, kBN, 0u, PHASE == MO_PHASE_UPDATE ? 1u : 0u);
-      int stage = 0;
-      uint32_t ph = 0;
-      int acc = 0;
-      uint32_t aph = 0;
-      bool issued = false;
-      bool ok = true;
-      for (int t = int(blockIdx.x); ok && t < p.ntiles; t += int(gridDim.x)) {
-        const TileRec tr = p.tiles[t];
-        const DevMat& M = p.mats[tr.mat];
-        const int K = (PHASE == MO_PHASE_GRAM) ? M.n : M.m;
-        const int nk = (K + kBK - 1) / kBK;
-        if (!mbar_wait_bounded(tempty_bar(acc), aph ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
-        ptx::tc_fence_after();
-        const uint32_t d = tmem_base + uint32_t(acc) * uint32_t(kBN);
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), ph, abort_flag, p.status, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t sa = base + uint32_t(stage) * kStageBytes;
-          const uint32_t sb = sa + kTileABytes;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = ptx::smem_desc_sw128(sa + uint32_t(kk) * 32u, 16u, 1024u);
-            const uint64_t bd = (PHASE == MO_PHASE_UPDATE)
-                                    ? ptx::smem_desc_sw128(sb + uint32_t(kk) * 2048u, kBoxBytes, 1024u)
-                                    : ptx::smem_desc_sw128(sb + uint32_t(kk) * 32u, 16u, 1024u);
-            ptx::umma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
-          ptx::umma_commit(empty_bar(stage));
-          issued = true;
-          if (++stage == kStages) {
-            stage = 0;
-            ph ^= 1u;
-          }
-        }
-        if (!ok) break;
-        ptx::umma_commit(tfull_bar(acc));
-        acc ^= 1;
-        if (acc == 0) aph ^= 1u;
-      }
-      if (*abort_flag && issued) {
-        ptx::umma_commit(drain_bar);
-        mbar_wait_drain(drain_bar, 0u, p.timeout_ns);
-      }
-    }
-  } else {
-    // -------------------------------------------------------------- epilogue
-    // warps 2..9: TMEM lane quarter = warp % 4, column half = (warp - 2) / 4
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int r_in = quarter * 32 + lane;
-    int acc = 0;
-    uint32_t aph = 0;
-    for (int t = int(blockIdx.x); t < p.ntiles; t += int(gridDim.x)) {
-      const TileRec tr = p.tiles[t];
-      const DevMat& M = p.mats[tr.mat];
-      bool ok = mbar_wait_bounded(tfull_bar(acc), aph, abort_flag, p.status, p.timeout_ns);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      const int row = int(tr.tm) * kBM + r_in;
-      const int cbase = int(tr.tn) * kBN + half * kEpiCols;
-      const uint32_t tb = tmem_base + uint32_t(acc) * uint32_t(kBN) + uint32_t(half * kEpiCols) +
-                          (uint32_t(quarter * 32) << 16);
-      if (PHASE == MO_PHASE_UPDATE)
-        epilogue_update<LAST>(p, M, row, cbase, tb);
-      else
-        epilogue_symmetric<PHASE>(p, M, row, cbase, tb);
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty_bar(acc));
-      acc ^= 1;
-      if (acc == 0) aph ^= 1u;
-    }
-  }
-
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
-}
-
 // ------------------------------------------------------------------ CTA-pair kernel
 //
 // Same three products with 256 x 256 output tiles computed by a cluster of
@@ -439,7 +261,9 @@ constexpr int kPairStages = 6;
 constexpr uint32_t kPairHalfBytes = 128 * kBK * 2;                  // 16 KB
 constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;            // A half + B half
 constexpr uint32_t kPairNumBars = 2 * kPairStages + 5;
-constexpr size_t kPairSmem = 1024 + size_t(kPairStages) * kPairStageBytes + 8 * kPairNumBars + 16;
+constexpr uint32_t kPairCtrlBytes = 256;                            // barriers, TMEM slot, abort flag
+static_assert(8 * kPairNumBars + 16 <= kPairCtrlBytes, "control block");
+constexpr size_t kPairSmem = 1024 + size_t(kPairStages) * kPairStageBytes + kPairCtrlBytes;
 
 template <int PHASE, bool LAST>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_constant__ NsParams p) {
@@ -622,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
     for (int t = cid; t < p.ntiles; t += ncl) {
       const TileRec tr = p.tiles[t];
       const DevMat& M = p.mats[tr.mat];
+      if (LAST) prefetch_w_rows(M, int(tr.tm) * 256 + int(rank) * 128 + r_in, int(tr.tn) * kBN + half * kEpiCols);
       bool ok = mbar_wait_bounded(tfull_bar(acc), aph, abort_flag, p.status, p.timeout_ns);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
@@ -688,20 +513,11 @@ cudaError_t launch_pair(const NsParams& p, int grid, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int PHASE, bool LAST>
-cudaError_t launch_one(const NsParams& p, int grid, cudaStream_t stream) {
-  auto kern = ns_gemm_kernel<PHASE, LAST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kGemmSmem));
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, kGemmSmem, stream>>>(p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
-size_t ns_gemm_smem_bytes() { return kGemmSmem; }
+size_t ns_gemm_smem_bytes() { return kPairSmem; }
 
-cudaError_t launch_ns_phase_pair(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream) {
   if (p.ntiles <= 0) return cudaSuccess;
   switch (phase) {
     case MO_PHASE_GRAM:
@@ -711,19 +527,6 @@ cudaError_t launch_ns_phase_pair(int phase, bool last, const NsParams& p, int gr
     default:
       return last ? launch_pair<MO_PHASE_UPDATE, true>(p, grid, stream)
                   : launch_pair<MO_PHASE_UPDATE, false>(p, grid, stream);
-  }
-}
-
-cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream) {
-  if (p.ntiles <= 0) return cudaSuccess;
-  switch (phase) {
-    case MO_PHASE_GRAM:
-      return launch_one<MO_PHASE_GRAM, false>(p, grid, stream);
-    case MO_PHASE_POLY:
-      return launch_one<MO_PHASE_POLY, false>(p, grid, stream);
-    default:
-      return last ? launch_one<MO_PHASE_UPDATE, true>(p, grid, stream)
-                  : launch_one<MO_PHASE_UPDATE, false>(p, grid, stream);
   }
 }
 
