@@ -62,8 +62,110 @@ int device_info(DeviceInfo** out) {
   return MO_OK;
 }
 
-int muon_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* ws, size_t ws_bytes,
-              cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
+// ---------------------------------------------------------------- plan cache
+//
+// Planning a table (tile schedules, tensor maps, header image) costs about a
+// millisecond of host time for the GPT-2 Large table and ~20 ms for a Llama
+// 8B table, so plans are cached per (device, table, workspace address). A hit
+// only re-uploads the immutable header image, from pinned memory when
+// available. The header is uploaded on every call, so the workspace contents
+// between calls never matter.
+struct PlanEntry {
+  int dev = -1;
+  std::vector<mo_matrix> table;
+  uintptr_t ws = 0;
+  mo::MuonLayout L;                  // offsets and schedules (pointers bound to `ws`)
+  std::vector<uint8_t> header;       // pageable header image
+  void* pinned = nullptr;            // pinned copy of the header, or null
+  cudaEvent_t uploaded = nullptr;    // recorded after the latest upload from `pinned`
+  uint64_t last_use = 0;
+};
+
+constexpr size_t kPlanCacheEntries = 8;
+std::mutex g_plan_mu;
+std::vector<PlanEntry*> g_plans;
+uint64_t g_plan_clock = 0;
+
+bool same_table(const PlanEntry& e, int dev, const mo_matrix* tbl, int32_t n, const void* ws) {
+  return e.dev == dev && e.ws == reinterpret_cast<uintptr_t>(ws) && e.table.size() == size_t(n) &&
+         std::memcmp(e.table.data(), tbl, sizeof(mo_matrix) * size_t(n)) == 0;
+}
+
+void free_entry(PlanEntry* e) {
+  if (e->uploaded) {
+    cudaEventSynchronize(e->uploaded);   // the pinned image may still be in flight
+    cudaEventDestroy(e->uploaded);
+  }
+  if (e->pinned) cudaFreeHost(e->pinned);
+  delete e;
+}
+
+// Binds a planned layout to `ws` and builds the header image.
+int build_entry(PlanEntry& E, const mo_matrix* tbl, int32_t n, void* ws) {
+  mo::MuonLayout& L = E.L;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  E.header.assign(L.header_bytes, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    mo::DevMat& d = L.mats[size_t(i)];
+    d.X[0] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[0]));
+    d.X[1] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[1]));
+    d.A = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.A));
+    d.B = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.B));
+    if (!mo::encode_matrix_maps(d, E.header.data() + L.off_tmaps + size_t(i) * mo::kMapsPerMat * mo::kTensorMapBytes))
+      return cuda_fail(cudaErrorInvalidValue);
+  }
+  std::memcpy(E.header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * size_t(n));
+  std::memcpy(E.header.data() + L.off_seg_prefix, L.seg_prefix.data(), sizeof(int64_t) * L.seg_prefix.size());
+  std::memcpy(E.header.data() + L.off_seg_code, L.seg_code.data(), sizeof(int32_t) * L.seg_code.size());
+  for (int ph = 0; ph < 3; ++ph)
+    if (!L.tiles[ph].empty())
+      std::memcpy(E.header.data() + L.off_tiles[ph], L.tiles[ph].data(), sizeof(mo::TileRec) * L.tiles[ph].size());
+  E.table.assign(tbl, tbl + n);
+  E.ws = reinterpret_cast<uintptr_t>(ws);
+  return MO_OK;
+}
+
+PlanEntry* find_plan(int dev, const mo_matrix* tbl, int32_t n, const void* ws) {
+  for (PlanEntry* e : g_plans)
+    if ((dev < 0 || e->dev == dev) && same_table(*e, e->dev, tbl, n, ws)) return e;
+  return nullptr;
+}
+
+// Inserts a freshly planned entry (caller holds g_plan_mu), evicting the least
+// recently used one when the cache is full.
+int insert_plan(PlanEntry* e, const mo_matrix* tbl, int32_t n, void* ws, bool want_pinned) {
+  const int st = build_entry(*e, tbl, n, ws);
+  if (st != MO_OK) return st;
+  e->pinned = nullptr;
+  e->uploaded = nullptr;
+  if (want_pinned && cudaHostAlloc(&e->pinned, e->header.size(), cudaHostAllocDefault) == cudaSuccess) {
+    std::memcpy(e->pinned, e->header.data(), e->header.size());
+    if (cudaEventCreateWithFlags(&e->uploaded, cudaEventDisableTiming) != cudaSuccess) {
+      e->uploaded = nullptr;
+      cudaFreeHost(e->pinned);
+      e->pinned = nullptr;
+    }
+  } else {
+    e->pinned = nullptr;
+    (void)cudaGetLastError();
+  }
+  if (g_plans.size() >= kPlanCacheEntries) {
+    size_t victim = 0;
+    for (size_t i = 1; i < g_plans.size(); ++i)
+      if (g_plans[i]->last_use < g_plans[victim]->last_use) victim = i;
+    free_entry(g_plans[victim]);
+    g_plans.erase(g_plans.begin() + long(victim));
+  }
+  g_plans.push_back(e);
+  return MO_OK;
+}
+
+}  // namespace
+
+namespace mo {
+
+int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* ws, size_t ws_bytes,
+                   cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end, bool allow_pinned) {
   int st = mo::validate_muon_params(prm);
   if (st != MO_OK) return st;
   if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
@@ -75,54 +177,70 @@ int muon_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* 
   }
   if (!ws) return MO_ERR_NULL_POINTER;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MO_ERR_MISALIGNED;
-  mo::MuonLayout L;
-  mo::plan_muon(tbl, n, mo::kBM, L);
-  if (ws_bytes < L.total_bytes) return MO_ERR_WORKSPACE_TOO_SMALL;
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != MO_OK) return st;
 
-  // bind workspace offsets to addresses and build the header image
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  std::vector<uint8_t> header(L.header_bytes, 0);
-  for (int32_t i = 0; i < n; ++i) {
-    mo::DevMat& d = L.mats[size_t(i)];
-    d.X[0] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[0]));
-    d.X[1] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[1]));
-    d.A = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.A));
-    d.B = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.B));
-    if (!mo::encode_matrix_maps(d, header.data() + L.off_tmaps + size_t(i) * mo::kMapsPerMat * mo::kTensorMapBytes))
-      return cuda_fail(cudaErrorInvalidValue);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  // Host-only part first: a rejected call makes no CUDA call.
+  PlanEntry* E = find_plan(-1, tbl, n, ws);
+  PlanEntry* fresh = nullptr;
+  if (E == nullptr) {
+    fresh = new PlanEntry();
+    mo::plan_muon(tbl, n, mo::kBM, fresh->L);
   }
-  std::memcpy(header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * size_t(n));
-  std::memcpy(header.data() + L.off_nrm_prefix, L.nrm_prefix.data(), sizeof(int64_t) * (size_t(n) + 1));
-  std::memcpy(header.data() + L.off_cast_prefix, L.cast_prefix.data(), sizeof(int64_t) * (size_t(n) + 1));
-  for (int ph = 0; ph < 3; ++ph)
-    if (!L.tiles[ph].empty())
-      std::memcpy(header.data() + L.off_tiles[ph], L.tiles[ph].data(), sizeof(mo::TileRec) * L.tiles[ph].size());
-
-  cudaError_t e = cudaMemcpyAsync(ws, header.data(), L.header_bytes, cudaMemcpyHostToDevice, stream);
+  const size_t need = (E ? E->L : fresh->L).total_bytes;
+  if (ws_bytes < need) {
+    delete fresh;
+    return MO_ERR_WORKSPACE_TOO_SMALL;
+  }
+  DeviceInfo* dev = nullptr;
+  int dev_id = 0;
+  if ((st = device_info(&dev)) != MO_OK || cudaGetDevice(&dev_id) != cudaSuccess) {
+    delete fresh;
+    return st != MO_OK ? st : cuda_fail(cudaErrorInvalidDevice);
+  }
+  if (E != nullptr && E->dev != dev_id) {
+    // same addresses on another device: look for that device's entry
+    E = find_plan(dev_id, tbl, n, ws);
+    if (E == nullptr) {
+      fresh = new PlanEntry();
+      mo::plan_muon(tbl, n, mo::kBM, fresh->L);
+    }
+  }
+  if (E == nullptr) {
+    fresh->dev = dev_id;
+    if ((st = insert_plan(fresh, tbl, n, ws, allow_pinned)) != MO_OK) {
+      delete fresh;
+      return st;
+    }
+    E = fresh;
+  }
+  E->last_use = ++g_plan_clock;
+  const mo::MuonLayout& L = E->L;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const bool use_pinned = allow_pinned && E->pinned != nullptr;
+  cudaError_t e = cudaMemcpyAsync(ws, use_pinned ? E->pinned : static_cast<const void*>(E->header.data()),
+                                  L.header_bytes, cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return cuda_fail(e);
+  if (use_pinned && (e = cudaEventRecord(E->uploaded, stream)) != cudaSuccess) return cuda_fail(e);
 
   const mo::DevMat* d_mats = reinterpret_cast<const mo::DevMat*>(wsb + L.off_meta);
   float* d_scales = reinterpret_cast<float*>(wsb + L.off_scales);
 
   mo::ProParams pp{};
   pp.mats = d_mats;
-  pp.nrm_prefix = reinterpret_cast<const int64_t*>(wsb + L.off_nrm_prefix);
-  pp.cast_prefix = reinterpret_cast<const int64_t*>(wsb + L.off_cast_prefix);
+  pp.seg_prefix = reinterpret_cast<const int64_t*>(wsb + L.off_seg_prefix);
+  pp.seg_code = reinterpret_cast<const int32_t*>(wsb + L.off_seg_code);
   pp.partials = reinterpret_cast<float*>(wsb + L.off_partials);
   pp.counters = reinterpret_cast<uint32_t*>(wsb + L.off_counters);
+  pp.ready = reinterpret_cast<uint32_t*>(wsb + L.off_ready);
+  pp.abort = reinterpret_cast<uint32_t*>(wsb + L.off_abort);
   pp.scales = d_scales;
-  pp.n = n;
-  pp.nrm_total = L.nrm_total;
-  pp.cast_total = L.cast_total;
+  pp.status = dev->status;
+  pp.nseg = int32_t(L.seg_code.size());
+  pp.total_items = L.seg_prefix.back();
   pp.mu = prm->mu;
   pp.eps = prm->eps;
-  const int64_t ew_grid = int64_t(dev->sms) * 8;
-  if ((e = mo::launch_muon_momentum_norm(pp, int(std::min<int64_t>(L.nrm_total, ew_grid)), stream)) != cudaSuccess)
-    return cuda_fail(e);
-  if ((e = mo::launch_muon_normalize_cast(pp, int(std::min<int64_t>(L.cast_total, ew_grid)), stream)) != cudaSuccess)
-    return cuda_fail(e);
+  pp.timeout_ns = 2000000000ull;
+  if ((e = mo::launch_muon_prologue(pp, 0, stream)) != cudaSuccess) return cuda_fail(e);
   if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) return cuda_fail(e);
 
   mo::NsParams np{};
@@ -150,6 +268,10 @@ int muon_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* 
   if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return cuda_fail(e);
   return MO_OK;
 }
+
+}  // namespace mo
+
+namespace {
 
 int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmnp_params* prm,
               cudaStream_t stream) {
@@ -213,12 +335,12 @@ size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_pa
 
 int muon_owner_step(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws, size_t ws_bytes,
                     cudaStream_t stream) {
-  return muon_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr);
+  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr, true);
 }
 
 int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws,
                           size_t ws_bytes, cudaStream_t stream, cudaEvent_t ev_ns_begin, cudaEvent_t ev_ns_end) {
-  return muon_impl(tbl, n, params, ws, ws_bytes, stream, ev_ns_begin, ev_ns_end);
+  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, ev_ns_begin, ev_ns_end, true);
 }
 
 int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cudaStream_t stream) {

@@ -5,6 +5,8 @@
 // a multiple of the SM count.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "kernels.h"
 #include "mo_internal.h"
@@ -21,43 +23,52 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // ------------------------------------------------------------------ Muon prologue
 //
-// Pass 1: momentum V <- mu V + G ("Optimizers In A Sharded World", section 1)
-// over flat 8192-element chunks of each stored matrix, with one fp32 sum of
-// squares per chunk. The CTA that completes a matrix's last chunk sums that
-// matrix's partials in a fixed order (deterministic, no float atomics) and
-// writes the Frobenius scale 1 / (||V|| + eps) (the appendix of the same page:
-// eps is added to the norm).
-__global__ void __launch_bounds__(256, 4) muon_momentum_norm_kernel(const __grid_constant__ ProParams p) {
-  __shared__ float red[8];
-  __shared__ int last_flag;
+// One persistent cooperative launch over a work list of two item kinds:
+//   norm items   momentum V <- mu V + G ("Optimizers In A Sharded World",
+//                section 1) over a flat 8192-element chunk of a stored
+//                matrix, with one fp32 sum of squares per chunk. The CTA that
+//                completes a matrix's last chunk sums that matrix's partials
+//                in a fixed order (deterministic, no float atomics), writes
+//                the Frobenius scale 1 / (||V|| + eps) (eps added to the norm,
+//                as in the same page's appendix) and marks the matrix ready.
+//   cast items   X0 = bf16(V * scale) for a 64 x 128 tile, written in the wide
+//                orientation (transposed through shared memory when
+//                rows > cols, appendix of the same page).
+// The list interleaves matrices (norm 0, norm 1, cast 0, norm 2, cast 1, ...)
+// so a matrix is cast while its fresh momentum is still in L2. A cast item
+// waits (bounded) for its matrix to be ready; every dependency points to an
+// earlier item, and all CTAs are co-resident, so the waits always end.
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ void prologue_norm_item(const ProParams& p, int mi, int64_t local, float* red, int* last_flag) {
   const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
-  for (int64_t t = blockIdx.x; t < p.nrm_total; t += gridDim.x) {
-    int lo = 0, hi = p.n - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.nrm_prefix[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    const int mi = lo;
-    const DevMat& M = p.mats[mi];
-    const int64_t e0 = (t - p.nrm_prefix[mi]) * kNrmChunk;
-    const int64_t left = int64_t(M.R) * int64_t(M.C) - e0;
-    const int cnt = left < kNrmChunk ? int(left) : int(kNrmChunk);   // elements in this chunk
-    float* __restrict__ V = M.V + e0;
-    const uint16_t* __restrict__ G = M.G + e0;
+  const DevMat& M = p.mats[mi];
+  const int64_t e0 = local * kNrmChunk;
+  const int64_t left = int64_t(M.R) * int64_t(M.C) - e0;
+  const int cnt = left < kNrmChunk ? int(left) : int(kNrmChunk);
+  float* __restrict__ V = M.V + e0;
+  const uint16_t* __restrict__ G = M.G + e0;
+  float ss = 0.f;
+#pragma unroll 1
+  for (int base = 0; base < cnt; base += 8 * 256 * 4) {
     float4 v[8];
     uint2 g[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int e = (j * 256 + tid) * 4;
+      const int e = base + (j * 256 + tid) * 4;
       if (e + 4 <= cnt) {
         v[j] = *reinterpret_cast<const float4*>(V + e);
         g[j] = *reinterpret_cast<const uint2*>(G + e);
       }
     }
-    float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int e = (j * 256 + tid) * 4;
+      const int e = base + (j * 256 + tid) * 4;
       if (e + 4 <= cnt) {
         float4 n4;
         n4.x = fmaf(p.mu, v[j].x, bf16_bits_to_float(g[j].x & 0xFFFFu));
@@ -77,121 +88,155 @@ __global__ void __launch_bounds__(256, 4) muon_momentum_norm_kernel(const __grid
         }
       }
     }
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    p.partials[M.nrm_base + local] = tot;
+    __threadfence();
+    const uint32_t prev = atomicAdd(&p.counters[mi], 1u);
+    *last_flag = (int64_t(prev) + 1 == M.nrm_count) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*last_flag) {
+    __threadfence();
+    float acc = 0.f;
+    for (int64_t k = tid; k < M.nrm_count; k += 256) acc += __ldcg(p.partials + M.nrm_base + k);
+    acc = warp_sum(acc);
+    if (lane == 0) red[warp] = acc;
     __syncthreads();
     if (tid == 0) {
       float tot = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) tot += red[w];
-      p.partials[t] = tot;
+      p.scales[mi] = 1.0f / (sqrtf(tot) + p.eps);
+      p.counters[mi] = 0u;
       __threadfence();
-      const uint32_t prev = atomicAdd(&p.counters[mi], 1u);
-      last_flag = (int64_t(prev) + 1 == M.nrm_count) ? 1 : 0;
+      atomicExch(&p.ready[mi], 1u);
+    }
+  }
+  __syncthreads();
+}
+
+// Thread 0 waits for the matrix's scale; returns false (for the whole CTA)
+// if the wait gave up or another CTA of the launch already gave up.
+__device__ bool prologue_wait_ready(const ProParams& p, int mi, int* ok_flag) {
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    if (ld_acquire(&p.ready[mi]) == 0u) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (true) {
+        if (ld_acquire(&p.ready[mi]) != 0u) break;
+        if (ld_acquire(p.abort) != 0u) { ok = 0; break; }
+        if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+          atomicExch(p.abort, 1u);
+          atomicExch(p.status, MO_ERR_DEVICE_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    *ok_flag = ok;
+  }
+  __syncthreads();
+  return *ok_flag != 0;
+}
+
+__device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, uint16_t (*tbuf)[kCastTR + 8]) {
+  const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
+  const DevMat& M = p.mats[mi];
+  const int r0 = int(local / M.cast_tiles_c) * kCastTR;
+  const int c0 = int(local % M.cast_tiles_c) * kCastTC;
+  const int R = M.R, C = M.C;
+  const float sc = __ldcg(p.scales + mi);
+  uint16_t* X = M.X[0];
+  const size_t ldx = size_t(M.ldx);
+  if (!M.tall) {
+    // warp w covers rows w, w+8, ...; lanes cover 4 consecutive columns each
+    const int c = c0 + lane * 4;
+#pragma unroll 4
+    for (int i = 0; i < kCastTR / 8; ++i) {
+      const int r = r0 + warp + 8 * i;
+      if (r >= R || c >= C) continue;
+      const size_t off = size_t(r) * size_t(C) + size_t(c);
+      uint16_t* xp = X + size_t(r) * ldx + size_t(c);
+      if (M.vec_ok && c + 4 <= C) {
+        const float4 v4 = __ldcg(reinterpret_cast<const float4*>(M.V + off));
+        *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16x2(v4.x * sc, v4.y * sc), pack_bf16x2(v4.z * sc, v4.w * sc));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < C) xp[q] = float_to_bf16_bits(__ldcg(M.V + off + q) * sc);
+      }
+    }
+  } else {
+    // X is [C, R]: X[c][r] = bf16(V[r][c] * scale). Thread = (row rl, 32-column
+    // quarter cq): lanes hold consecutive rows, so the shared-memory writes
+    // tbuf[c][rl] of a warp are contiguous; each lane reads its 128-byte row
+    // segment with 32-byte vectors.
+    const int rl = tid & (kCastTR - 1);
+    const int cq = tid >> 6;
+    const int r = r0 + rl;
+    const int cb = cq * 32;
+    if (r < R) {
+      const float* vrow = M.V + size_t(r) * size_t(C) + size_t(c0 + cb);
+      if (c0 + cb + 32 <= C && (reinterpret_cast<uintptr_t>(vrow) & 31u) == 0) {
+        uint32_t w8[4][8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ptx::ld_global_v8_cg(vrow + 8 * j, w8[j]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) tbuf[cb + 8 * j + q][rl] = float_to_bf16_bits(__uint_as_float(w8[j][q]) * sc);
+      } else {
+        for (int j = 0; j < 32; ++j)
+          tbuf[cb + j][rl] = (c0 + cb + j < C) ? float_to_bf16_bits(__ldcg(vrow + j) * sc) : uint16_t(0);
+      }
     }
     __syncthreads();
-    if (last_flag) {
-      __threadfence();
-      float acc = 0.f;
-      for (int64_t k = tid; k < M.nrm_count; k += 256) acc += __ldcg(p.partials + M.nrm_base + k);
-      acc = warp_sum(acc);
-      if (lane == 0) red[warp] = acc;
-      __syncthreads();
-      if (tid == 0) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) tot += red[w];
-        p.scales[mi] = 1.0f / (sqrtf(tot) + p.eps);
-        p.counters[mi] = 0u;
+    // 16-byte segments of 8 rows per X row
+    for (int k = tid; k < kCastTC * (kCastTR / 8); k += 256) {
+      const int cc = k >> 3, seg = k & 7;
+      const int xc = c0 + cc;
+      const int xr = r0 + seg * 8;
+      if (xc < C && xr < R) {
+        uint16_t* xp = X + size_t(xc) * ldx + size_t(xr);
+        const uint16_t* sp = &tbuf[cc][seg * 8];
+        if (xr + 8 <= R) {
+          *reinterpret_cast<uint4*>(xp) = *reinterpret_cast<const uint4*>(sp);
+        } else {
+          for (int j = 0; j < 8; ++j)
+            if (xr + j < R) xp[j] = sp[j];
+        }
       }
     }
     __syncthreads();
   }
 }
 
-// Pass 2: X0 = bf16(V * scale), written in the wide orientation: X = V for
-// rows <= cols, X = V^T (through a shared-memory transpose) otherwise
-// (appendix of "Optimizers In A Sharded World": transpose when rows > cols).
-// 64 x 128 tiles of the stored matrix; X rows are padded to ldx.
-__global__ void __launch_bounds__(256) muon_normalize_cast_kernel(const __grid_constant__ ProParams p) {
+__global__ void __launch_bounds__(256, 4) muon_prologue_kernel(const __grid_constant__ ProParams p) {
   __shared__ __align__(16) uint16_t tbuf[kCastTC][kCastTR + 8];
-  const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
-  for (int64_t t = blockIdx.x; t < p.cast_total; t += gridDim.x) {
-    int lo = 0, hi = p.n - 1;
+  __shared__ float red[8];
+  __shared__ int flag;
+  for (int64_t t = blockIdx.x; t < p.total_items; t += gridDim.x) {
+    int lo = 0, hi = p.nseg - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.cast_prefix[mid] <= t) lo = mid; else hi = mid - 1;
+      if (p.seg_prefix[mid] <= t) lo = mid; else hi = mid - 1;
     }
-    const int mi = lo;
-    const DevMat& M = p.mats[mi];
-    const int64_t local = t - p.cast_prefix[mi];
-    const int r0 = int(local / M.cast_tiles_c) * kCastTR;
-    const int c0 = int(local % M.cast_tiles_c) * kCastTC;
-    const int R = M.R, C = M.C;
-    const float sc = p.scales[mi];
-    uint16_t* X = M.X[0];
-    const size_t ldx = size_t(M.ldx);
-    if (!M.tall) {
-      // warp w covers rows w, w+8, ...; lanes cover 4 consecutive columns each
-      const int c = c0 + lane * 4;
-#pragma unroll 4
-      for (int i = 0; i < kCastTR / 8; ++i) {
-        const int r = r0 + warp + 8 * i;
-        if (r >= R || c >= C) continue;
-        const size_t off = size_t(r) * size_t(C) + size_t(c);
-        uint16_t* xp = X + size_t(r) * ldx + size_t(c);
-        if (M.vec_ok && c + 4 <= C) {
-          const float4 v4 = *reinterpret_cast<const float4*>(M.V + off);
-          *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16x2(v4.x * sc, v4.y * sc), pack_bf16x2(v4.z * sc, v4.w * sc));
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (c + q < C) xp[q] = float_to_bf16_bits(M.V[off + q] * sc);
-        }
-      }
+    const int code = p.seg_code[lo];
+    const int mi = code >> 1;
+    const int64_t local = t - p.seg_prefix[lo];
+    if ((code & 1) == 0) {
+      prologue_norm_item(p, mi, local, red, &flag);
     } else {
-      // X is [C, R]: X[c][r] = bf16(V[r][c] * scale). Thread = (row rl, 32-column
-      // quarter cq): lanes hold consecutive rows, so the shared-memory writes
-      // tbuf[c][rl] of a warp are contiguous.
-      const int rl = tid & (kCastTR - 1);
-      const int cq = tid >> 6;
-      const int r = r0 + rl;
-      const int cb = cq * 32;
-      if (r < R) {
-        const float* vrow = M.V + size_t(r) * size_t(C) + size_t(c0 + cb);
-        if (M.vec_ok && c0 + cb + 32 <= C) {
-          float4 v4[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v4[j] = reinterpret_cast<const float4*>(vrow)[j];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            tbuf[cb + 4 * j + 0][rl] = float_to_bf16_bits(v4[j].x * sc);
-            tbuf[cb + 4 * j + 1][rl] = float_to_bf16_bits(v4[j].y * sc);
-            tbuf[cb + 4 * j + 2][rl] = float_to_bf16_bits(v4[j].z * sc);
-            tbuf[cb + 4 * j + 3][rl] = float_to_bf16_bits(v4[j].w * sc);
-          }
-        } else {
-          for (int j = 0; j < 32; ++j) tbuf[cb + j][rl] = (c0 + cb + j < C) ? float_to_bf16_bits(vrow[j] * sc) : uint16_t(0);
-        }
-      }
-      __syncthreads();
-      // 16-byte segments of 8 rows per X row
-      for (int k = tid; k < kCastTC * (kCastTR / 8); k += 256) {
-        const int cc = k >> 3, seg = k & 7;
-        const int xc = c0 + cc;
-        const int xr = r0 + seg * 8;
-        if (xc < C && xr < R) {
-          uint16_t* xp = X + size_t(xc) * ldx + size_t(xr);
-          const uint16_t* sp = &tbuf[cc][seg * 8];
-          if (xr + 8 <= R) {
-            *reinterpret_cast<uint4*>(xp) = *reinterpret_cast<const uint4*>(sp);
-          } else {
-            for (int j = 0; j < 8; ++j)
-              if (xr + j < R) xp[j] = sp[j];
-          }
-        }
-      }
-      __syncthreads();
+      if (!prologue_wait_ready(p, mi, &flag)) return;   // uniform across the CTA
+      prologue_cast_item(p, mi, local, tbuf);
     }
   }
 }
@@ -351,16 +396,21 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
 
 }  // namespace
 
-cudaError_t launch_muon_momentum_norm(const ProParams& p, int grid, cudaStream_t stream) {
-  if (p.nrm_total <= 0) return cudaSuccess;
-  muon_momentum_norm_kernel<<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_muon_normalize_cast(const ProParams& p, int grid, cudaStream_t stream) {
-  if (p.cast_total <= 0) return cudaSuccess;
-  muon_normalize_cast_kernel<<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_muon_prologue(const ProParams& p, int max_grid, cudaStream_t stream) {
+  if (p.total_items <= 0) return cudaSuccess;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, muon_prologue_kernel, 256, 0)) != cudaSuccess)
+    return e;
+  int64_t grid = int64_t(sms) * int64_t(per_sm);
+  if (max_grid > 0) grid = std::min<int64_t>(grid, max_grid);
+  grid = std::max<int64_t>(1, std::min<int64_t>(grid, p.total_items));
+  ProParams copy = p;
+  void* args[] = {&copy};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(muon_prologue_kernel), dim3(unsigned(grid)),
+                                     dim3(256), args, 0, stream);
 }
 
 cudaError_t launch_rmnp(const RmnpParams& p, int grid, cudaStream_t stream) {

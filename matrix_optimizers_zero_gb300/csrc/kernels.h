@@ -34,18 +34,22 @@ cudaError_t launch_bounded_wait_selftest(int* status, uint64_t timeout_ns, cudaS
 // ---------------------------------------------------------------- Muon prologue
 struct ProParams {
   const DevMat* mats;
-  const int64_t* nrm_prefix;  // n + 1 prefix sums of sum-of-squares chunks
-  const int64_t* cast_prefix; // n + 1 prefix sums of normalise/cast tiles
+  const int64_t* seg_prefix;  // 2n + 1 prefix sums of the work-list segments
+  const int32_t* seg_code;    // 2n segment codes: matrix * 2 + kind
   float* partials;            // one sum of squares per chunk
   uint32_t* counters;         // per matrix, zero on entry, zero again on exit
-  float* scales;              // out of pass 1: 1 / (||V_new||_F + eps)
-  int32_t n;
-  int64_t nrm_total;
-  int64_t cast_total;
+  uint32_t* ready;            // per matrix, set once its scale is final (zero on entry)
+  uint32_t* abort;            // set when any wait of the launch expired (zero on entry)
+  float* scales;              // 1 / (||V_new||_F + eps)
+  int* status;                // device status word
+  int32_t nseg;
+  int64_t total_items;
   float mu, eps;
+  uint64_t timeout_ns;
 };
-cudaError_t launch_muon_momentum_norm(const ProParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_muon_normalize_cast(const ProParams& p, int grid, cudaStream_t stream);
+// Cooperative launch (all CTAs co-resident): normalise/cast items wait for
+// their matrix's norm, which only depends on earlier items of the list.
+cudaError_t launch_muon_prologue(const ProParams& p, int max_grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- RMNP
 constexpr int kRmnpMaxEntries = 512;

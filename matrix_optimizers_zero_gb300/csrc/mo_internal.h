@@ -16,10 +16,10 @@ constexpr int kBM = 256;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 
-// Muon prologue, pass 1 (momentum + sum of squares): flat chunks of the
-// row-major stored matrix. Pass 2 (normalise + bf16 cast, transposed for tall
+// Muon prologue norm items (momentum + sum of squares): flat chunks of the
+// row-major stored matrix; cast items (normalise + bf16 cast, transposed for tall
 // matrices): 64 x 128 tiles of the stored matrix.
-constexpr int64_t kNrmChunk = 8192;
+constexpr int64_t kNrmChunk = 32768;
 constexpr int kCastTR = 64;
 constexpr int kCastTC = 128;
 

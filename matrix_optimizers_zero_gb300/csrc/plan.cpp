@@ -146,8 +146,7 @@ void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector
 void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L) {
   L.n = n;
   L.mats.assign(size_t(n), DevMat{});
-  L.nrm_prefix.assign(size_t(n) + 1, 0);
-  L.cast_prefix.assign(size_t(n) + 1, 0);
+  std::vector<int64_t> chunks(static_cast<size_t>(n), 0), casts(static_cast<size_t>(n), 0);
   int64_t nrm = 0, cast = 0;
   for (int32_t i = 0; i < n; ++i) {
     DevMat& d = L.mats[size_t(i)];
@@ -167,15 +166,24 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L) {
     d.shape_scale = float(std::sqrt(std::max(1.0, double(R) / double(C))));
     d.nrm_base = nrm;
     d.nrm_count = ceil_div(R * C, kNrmChunk);
-    L.nrm_prefix[size_t(i)] = nrm;
-    L.cast_prefix[size_t(i)] = cast;
+    chunks[size_t(i)] = d.nrm_count;
+    casts[size_t(i)] = ceil_div(R, kCastTR) * ceil_div(C, kCastTC);
     nrm += d.nrm_count;
-    cast += ceil_div(R, kCastTR) * ceil_div(C, kCastTC);
+    cast += casts[size_t(i)];
   }
-  L.nrm_prefix[size_t(n)] = nrm;
-  L.cast_prefix[size_t(n)] = cast;
   L.nrm_total = nrm;
   L.cast_total = cast;
+  L.seg_code.clear();
+  for (int32_t i = 0; i < n; ++i) {
+    L.seg_code.push_back(2 * i);
+    if (i >= 1) L.seg_code.push_back(2 * (i - 1) + 1);
+  }
+  if (n >= 1) L.seg_code.push_back(2 * (n - 1) + 1);
+  L.seg_prefix.assign(L.seg_code.size() + 1, 0);
+  for (size_t k = 0; k < L.seg_code.size(); ++k) {
+    const int32_t mat = L.seg_code[k] >> 1;
+    L.seg_prefix[k + 1] = L.seg_prefix[k] + ((L.seg_code[k] & 1) ? casts[size_t(mat)] : chunks[size_t(mat)]);
+  }
   for (int ph = 0; ph < 3; ++ph) build_tiles(tbl, n, ph, bm, L.tiles[ph]);
 
   size_t off = 0;
@@ -183,12 +191,16 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L) {
   off = align_up(off + sizeof(DevMat) * size_t(n), 128);
   L.off_tmaps = off;
   off = align_up(off + kTensorMapBytes * kMapsPerMat * size_t(n), 256);
-  L.off_nrm_prefix = off;
-  off = align_up(off + sizeof(int64_t) * (size_t(n) + 1), 256);
-  L.off_cast_prefix = off;
-  off = align_up(off + sizeof(int64_t) * (size_t(n) + 1), 256);
+  L.off_seg_prefix = off;
+  off = align_up(off + sizeof(int64_t) * L.seg_prefix.size(), 256);
+  L.off_seg_code = off;
+  off = align_up(off + sizeof(int32_t) * L.seg_code.size(), 256);
   L.off_counters = off;
   off = align_up(off + sizeof(uint32_t) * size_t(n), 256);
+  L.off_ready = off;
+  off = align_up(off + sizeof(uint32_t) * size_t(n), 256);
+  L.off_abort = off;
+  off = align_up(off + sizeof(uint32_t), 256);
   for (int ph = 0; ph < 3; ++ph) {
     L.off_tiles[ph] = off;
     off = align_up(off + sizeof(TileRec) * L.tiles[ph].size(), 256);

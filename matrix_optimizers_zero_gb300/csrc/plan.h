@@ -14,12 +14,17 @@ namespace mo {
 struct MuonLayout {
   int32_t n = 0;
   std::vector<DevMat> mats;          // buffer pointers hold workspace OFFSETS until bound
-  std::vector<int64_t> nrm_prefix;   // n + 1 prefix sums of sum-of-squares chunks
-  std::vector<int64_t> cast_prefix;  // n + 1 prefix sums of normalise/cast tiles
+  // Prologue work list: 2n segments in the order momentum/norm chunks of
+  // matrix 0, of matrix 1, normalise/cast tiles of matrix 0, chunks of
+  // matrix 2, tiles of matrix 1, ... so that a matrix is cast right after its
+  // norm is final (while its momentum is still in L2).
+  std::vector<int64_t> seg_prefix;   // 2n + 1 prefix sums of segment sizes
+  std::vector<int32_t> seg_code;     // 2n codes: matrix * 2 + (0 = norm chunks, 1 = cast tiles)
   std::vector<TileRec> tiles[3];     // per phase, launch order
   int64_t nrm_total = 0;
   int64_t cast_total = 0;
-  size_t off_meta = 0, off_tmaps = 0, off_nrm_prefix = 0, off_cast_prefix = 0, off_counters = 0;
+  size_t off_meta = 0, off_tmaps = 0, off_seg_prefix = 0, off_seg_code = 0, off_counters = 0, off_ready = 0,
+         off_abort = 0;
   size_t off_tiles[3] = {0, 0, 0};
   size_t header_bytes = 0;           // [0, header_bytes) is uploaded by every call
   size_t off_partials = 0, off_scales = 0, off_buffers = 0;
