@@ -203,6 +203,36 @@ enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
 int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase,
                           mo_tile* out, int64_t cap, int64_t* count);
 
+/* ---- owner planning ("MatrixFSDP", section 4.1, Algorithm 1) ----
+ * A role is one 2D matrix or the packed non-matrix tail of one block. The
+ * planner assigns every role whole to one of `world` owner ranks, balancing
+ * the owner-resident element count (the load). Host only; no CUDA call.
+ *   MO_PLAN_ROLE_GREEDY   blocks in increasing block id; within a block the
+ *                         roles in decreasing numel (ties: table order), each
+ *                         to the currently lightest rank (ties: lowest rank);
+ *                         loads carry across blocks.
+ *   MO_PLAN_SCOPE_GREEDY  all roles pooled in decreasing numel (ties: table
+ *                         order), each to the lightest rank.
+ *   MO_PLAN_COST_AWARE    ScopeGreedy if its max/avg load ratio is strictly
+ *                         lower than RoleGreedy's and no rank owns more than
+ *                         `block_cap` elements within one block (block_cap <= 0:
+ *                         no cap); RoleGreedy otherwise.
+ * owner_out[nroles] receives the owner of each role, load_out[world] (may be
+ * NULL) the per-rank loads, chosen_out (may be NULL) the strategy applied.
+ * Returns MO_ERR_BAD_PARAM for an unknown strategy or world < 1,
+ * MO_ERR_BAD_SHAPE for negative numel or block ids, MO_ERR_NULL_POINTER for
+ * missing arrays. */
+typedef struct {
+  int64_t numel;   /* elements of the role (>= 0) */
+  int32_t block;   /* FSDP block (wrap unit) the role belongs to (>= 0) */
+  int32_t is_tail; /* 1 for a block's packed non-matrix tail, 0 for a matrix */
+} mo_role;
+
+enum mo_plan_strategy { MO_PLAN_ROLE_GREEDY = 0, MO_PLAN_SCOPE_GREEDY = 1, MO_PLAN_COST_AWARE = 2 };
+
+int mo_plan_owners(const mo_role* roles, int32_t nroles, int32_t world, int32_t strategy, int64_t block_cap,
+                   int32_t* owner_out, int64_t* load_out, int32_t* chosen_out);
+
 /* ---- diagnostics ---- */
 
 /* Launches one CTA that waits on a barrier nothing will complete, with a

@@ -20,7 +20,7 @@ __all__ = [
     "mo_muon_workspace_bytes", "muon_workspace", "muon_owner_step", "muon_owner_step_timed",
     "rmnp_step", "rmnp_step_scaled", "adamw_tail_step", "mo_last_device_error",
     "mo_status_string", "mo_selftest_bounded_wait", "mo_muon_tile_schedule", "MuonTable",
-    "TailTable", "RmnpTable", "muon_owner_step_noalloc", "mo_static_scratch_bytes",
+    "TailTable", "RmnpTable", "muon_owner_step_noalloc", "mo_static_scratch_bytes", "mo_plan_owners",
 ]
 
 MO_OK = 0
@@ -60,6 +60,13 @@ class AdamWParams(ctypes.Structure):
 
     def __init__(self, lr=1e-3, wd=1e-2, beta1=0.9, beta2=0.95, eps=1e-8, step=1):
         super().__init__(lr, wd, beta1, beta2, eps, step)
+
+
+class MoRole(ctypes.Structure):
+    _fields_ = [("numel", ctypes.c_int64), ("block", ctypes.c_int32), ("is_tail", ctypes.c_int32)]
+
+
+PLAN_ROLE_GREEDY, PLAN_SCOPE_GREEDY, PLAN_COST_AWARE = 0, 1, 2
 
 
 class MoTile(ctypes.Structure):
@@ -102,6 +109,7 @@ def load_library() -> ctypes.CDLL:
         "mo_muon_tile_schedule": (ctypes.c_int, [P, I32, I32, P, I64, P]),
         "mo_selftest_bounded_wait": (ctypes.c_int, [I64, P]),
         "muon_owner_step_noalloc": (ctypes.c_int, [P, I32, P, P]),
+        "mo_plan_owners": (ctypes.c_int, [P, I32, I32, I32, I64, P, P, P]),
         "mo_static_scratch_bytes": (SZ, []),
     }
     for name, (res, args) in sig.items():
@@ -293,3 +301,21 @@ def mo_muon_tile_schedule(shapes: Sequence[Tuple[int, int]], phase: int) -> List
                                      ctypes.cast(out, ctypes.c_void_p), count.value, ctypes.byref(count)),
            "mo_muon_tile_schedule")
     return [(t.mat, t.tm, t.tn) for t in out[:count.value]]
+
+
+# ---------------------------------------------------------------- owner planning
+
+def mo_plan_owners(roles: Sequence[Tuple[int, int, int]], world: int, strategy: int = PLAN_COST_AWARE,
+                   block_cap: int = 0):
+    """Owner assignment of roles (numel, block, is_tail) over `world` ranks.
+    Returns (owners, loads, chosen_strategy)."""
+    n = len(roles)
+    arr = (MoRole * max(1, n))(*[MoRole(int(a), int(b), int(c)) for a, b, c in roles])
+    owners = (ctypes.c_int32 * max(1, n))()
+    loads = (ctypes.c_int64 * max(1, world))()
+    chosen = ctypes.c_int32(-1)
+    _check(load_library().mo_plan_owners(ctypes.cast(arr, ctypes.c_void_p), n, int(world), int(strategy),
+                                         int(block_cap), ctypes.cast(owners, ctypes.c_void_p),
+                                         ctypes.cast(loads, ctypes.c_void_p), ctypes.byref(chosen)),
+           "mo_plan_owners")
+    return list(owners[:n]), list(loads[:world]), int(chosen.value)

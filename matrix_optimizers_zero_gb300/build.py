@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libmo.so")
-SOURCES = ["plan.cpp", "abi.cu", "elementwise.cu", "ns_gemm.cu", "static_ws.cu"]
+SOURCES = ["plan.cpp", "planner.cpp", "abi.cu", "elementwise.cu", "ns_gemm.cu", "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

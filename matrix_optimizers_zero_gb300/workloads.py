@@ -301,3 +301,21 @@ ADAMW_BYTES_PER_EL = 28          # p, m, v read + write (24) + g read (4)
 def workload_alg_flops(wl: Workload, steps: Optional[int] = None) -> int:
     st = wl.ns_steps if steps is None else steps
     return sum(ns_alg_flops(s.rows, s.cols, st) for s in wl.matrices)
+
+
+def owner_roles(wl: Workload, matrices_per_block: int) -> List[Tuple[int, int, int]]:
+    """Planner roles (numel, block, is_tail) of a table whose matrices come in
+    blocks of `matrices_per_block` (one transformer layer per block); each
+    block's tail role is its share of the tail segments, in order."""
+    nblocks = len(wl.matrices) // matrices_per_block
+    roles = []
+    for b in range(nblocks):
+        for s in wl.matrices[b * matrices_per_block:(b + 1) * matrices_per_block]:
+            roles.append((s.rows * s.cols, b, 0))
+    if wl.tail:
+        per = max(1, len(wl.tail) // max(1, nblocks))
+        for b in range(nblocks):
+            seg = wl.tail[b * per:(b + 1) * per] if b < nblocks - 1 else wl.tail[b * per:]
+            if seg:
+                roles.append((sum(seg), b, 1))
+    return roles

@@ -173,3 +173,26 @@ def test_bounded_wait_reports_timeout():
     # the context is still usable
     x = torch.ones(4, device=DEV)
     assert float((x * 2).sum()) == 8.0
+
+
+def test_plan_cache_alternating_tables_on_one_workspace():
+    """Plans are cached per (device, table, workspace address); alternating
+    two different tables on the same workspace must stay correct on every
+    call (each call re-uploads its own header)."""
+    wl1 = workloads.custom_workload([(130, 257), (64, 640)], g_std=1e-3)
+    wl2 = workloads.custom_workload([(257, 130), (300, 300), (512, 128)], g_std=1e-3, config_id=98)
+    t1 = to_device([workloads.host_matrix(wl1, i) for i in range(2)], DEV)
+    t2 = to_device([workloads.host_matrix(wl2, i) for i in range(3)], DEV)
+    p = mo.MuonParams()
+    nbytes = max(mo.mo_muon_workspace_bytes(t1, p), mo.mo_muon_workspace_bytes(t2, p))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    for tbl in (t1, t2, t1, t2, t1):
+        snap = [tuple(f64(x) for x in m) for m in tbl]
+        mo.muon_owner_step(tbl, p, ws)
+        torch.cuda.synchronize()
+        assert mo.mo_last_device_error() == 0
+        for (W0, G0, V0), (Wd, _, Vd) in zip(snap, tbl):
+            R, C = W0.shape
+            _, Vn, O = oracle.muon_matrix_step(W0, G0, V0, lr=p.lr, wd=p.wd, mu=p.mu)
+            assert max_rel(f64(Vd), Vn) <= FP32_MAX_REL_TOL
+            assert rel_frob(extract_update(W0, f64(Wd), p.lr, p.wd, R, C), O) <= NS_REL_FROB_TOL
