@@ -31,6 +31,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "owner Muon step ms & NS TFLOP/s vs bf16 peak; RMNP/AdamW HBM GB/s"
+
+# DRAM bytes of one step's 15 Newton-Schulz launches on the GPT-2 Large table,
+# from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the four-layer
+# table scaled x9 by matrices (profiles/ns_gemm_pair_gpt2l_4layers_full.md).
+# Valid only for the kernel source it was measured on.
+NS_TRAFFIC = {"source_sha256_16": "7891e1dd149fbf8d", "workload": "gpt2l", "bytes_per_ns_segment": 30.075e9}
 UNIT = "TFLOP/s"
 
 
@@ -43,6 +49,17 @@ def load_peaks():
                 "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def ns_traffic(workload: str):
+    """The profiled DRAM traffic of the NS launches, or None when the kernel
+    source differs from the one profiled (or for another workload)."""
+    import hashlib
+    path = os.path.join(ROOT, "matrix_optimizers_zero_gb300", "csrc", "ns_gemm.cu")
+    digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    if digest != NS_TRAFFIC["source_sha256_16"] or workload != NS_TRAFFIC["workload"]:
+        return None
+    return NS_TRAFFIC["bytes_per_ns_segment"]
 
 
 # ---------------------------------------------------------------- multi-rank helpers
@@ -375,12 +392,13 @@ def run_ours(args, rank, world, local_rank):
         },
         "roofline": {
             "bound": "tensor",
-            "kernel": "ns_gemm_kernel (Gram, A.A and B.X launches of all iterations)",
+            "kernel": "ns_gemm_pair_kernel (the 15 Gram, A.A and B.X launches of one step)",
             "achieved": round(ns_tflops, 2),
             "peak": peak,
             "unit": "TFLOP/s",
             "frac": round(ns_tflops / peak, 4),
-            "traffic": None,
+            "traffic": ns_traffic(wl.name),
+            "traffic_unit": "DRAM bytes per step's NS launches (ncu, 4-layer capture x9)",
             "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
         },
         "e2e": ({"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),

@@ -169,6 +169,23 @@ int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cud
 int rmnp_step_scaled(const mo_matrix* tbl, const float* scales, int32_t n,
                      const mo_rmnp_params* params, cudaStream_t stream);
 
+/* RMNP with rows cut into column shards ("Optimizers In A Sharded World",
+ * section 3, column-cut tensor parallelism, and the appendix's column-cut
+ * scheme), evaluated on one GPU: each table entry is one dense column shard
+ * [rows, cols_i] of a logical matrix; entries with equal group[i] are shards
+ * of the same matrix, must be consecutive in the table and have equal rows.
+ * Per shard: V <- mu V + G and the sum of squares of each of its rows; per
+ * row of a matrix, the shard partials are added in table order (the page's
+ * all-reduce); then every shard updates
+ *   W <- W (1 - lr wd) - lr scales[i] V / max(sqrt(total), eps).
+ * params->eps is the clamp (the page's scheme uses 1e-7). scales[i] is
+ * normally sqrt(max(1, rows / total_cols)) of the whole matrix.
+ * ws: device buffer of mo_rmnp_colcut_workspace_bytes() bytes (the per-row
+ * partial sums), 16-byte aligned. At most 512 entries per call. */
+size_t mo_rmnp_colcut_workspace_bytes(const mo_matrix* shards, int32_t n);
+int rmnp_colcut_step(const mo_matrix* shards, const int32_t* group, const float* scales, int32_t n,
+                     const mo_rmnp_params* params, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device-side status word:
  * MO_OK, or MO_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel expired
  * (the kernel then skipped its remaining work and released its resources). */

@@ -21,6 +21,7 @@ __all__ = [
     "rmnp_step", "rmnp_step_scaled", "adamw_tail_step", "mo_last_device_error",
     "mo_status_string", "mo_selftest_bounded_wait", "mo_muon_tile_schedule", "MuonTable",
     "TailTable", "RmnpTable", "muon_owner_step_noalloc", "mo_static_scratch_bytes", "mo_plan_owners",
+    "rmnp_colcut_step",
 ]
 
 MO_OK = 0
@@ -110,6 +111,8 @@ def load_library() -> ctypes.CDLL:
         "mo_selftest_bounded_wait": (ctypes.c_int, [I64, P]),
         "muon_owner_step_noalloc": (ctypes.c_int, [P, I32, P, P]),
         "mo_plan_owners": (ctypes.c_int, [P, I32, I32, I32, I64, P, P, P]),
+        "mo_rmnp_colcut_workspace_bytes": (SZ, [P, I32]),
+        "rmnp_colcut_step": (ctypes.c_int, [P, P, P, I32, P, P, SZ, P]),
         "mo_static_scratch_bytes": (SZ, []),
     }
     for name, (res, args) in sig.items():
@@ -256,6 +259,27 @@ def rmnp_step_scaled(mats, scales: Sequence[float], params: Optional[RmnpParams]
     arr = (ctypes.c_float * max(1, len(scales)))(*[float(s) for s in scales])
     _check(load_library().rmnp_step_scaled(t.ptr, ctypes.cast(arr, ctypes.c_void_p), t.n,
                                            ctypes.byref(params), _stream_ptr(stream)), "rmnp_step_scaled")
+
+
+def rmnp_colcut_step(shards, groups: Sequence[int], scales: Sequence[float], params: Optional[RmnpParams] = None,
+                     workspace=None, stream=None) -> None:
+    """Column-cut RMNP over column shards (W, G, V) of logical matrices;
+    shards with equal group ids belong to one matrix. `workspace` is a device
+    tensor of at least mo_rmnp_colcut_workspace_bytes bytes (allocated with
+    torch when None)."""
+    import torch
+    t = _as_table(shards)
+    params = params or RmnpParams(eps=1e-7)
+    lib = load_library()
+    nbytes = int(lib.mo_rmnp_colcut_workspace_bytes(t.ptr, t.n))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=t.keep[0][0].device)
+    g = (ctypes.c_int32 * max(1, t.n))(*[int(x) for x in groups])
+    sc = (ctypes.c_float * max(1, t.n))(*[float(x) for x in scales])
+    _check(lib.rmnp_colcut_step(t.ptr, ctypes.cast(g, ctypes.c_void_p), ctypes.cast(sc, ctypes.c_void_p), t.n,
+                                ctypes.byref(params), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "rmnp_colcut_step")
 
 
 def adamw_tail_step(segs, params: Optional[AdamWParams] = None, stream=None) -> None:

@@ -353,6 +353,67 @@ int rmnp_step_scaled(const mo_matrix* tbl, const float* scales, int32_t n, const
   return rmnp_impl(tbl, scales, n, params, stream);
 }
 
+size_t mo_rmnp_colcut_workspace_bytes(const mo_matrix* shards, int32_t n) {
+  if (mo::validate_matrix_table(shards, n) != MO_OK) return 0;
+  int64_t rows = 0;
+  for (int32_t i = 0; i < n; ++i) rows += shards[i].rows;
+  return size_t((rows * 4 + 255) / 256 * 256);
+}
+
+int rmnp_colcut_step(const mo_matrix* shards, const int32_t* group, const float* scales, int32_t n,
+                     const mo_rmnp_params* params, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int st = mo::validate_rmnp_params(params);
+  if (st != MO_OK) return st;
+  if ((st = mo::validate_matrix_table(shards, n)) != MO_OK) return st;
+  if (n > mo::kRmnpMaxEntries) return MO_ERR_BAD_SHAPE;
+  if (n == 0) return MO_OK;
+  if (!group || !scales || !ws) return MO_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) return MO_ERR_MISALIGNED;
+  for (int32_t i = 0; i < n; ++i) {
+    if (!std::isfinite(scales[i])) return MO_ERR_BAD_PARAM;
+    if (i > 0 && group[i] != group[i - 1]) {
+      for (int32_t j = 0; j < i; ++j)
+        if (group[j] == group[i]) return MO_ERR_BAD_PARAM;   // a group must be consecutive
+    }
+    if (i > 0 && group[i] == group[i - 1] && shards[i].rows != shards[i - 1].rows) return MO_ERR_BAD_SHAPE;
+  }
+  if (ws_bytes < mo_rmnp_colcut_workspace_bytes(shards, n)) return MO_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MO_OK) return st;
+  static thread_local mo::ColcutParams cp;
+  std::memset(&cp, 0, sizeof(cp));
+  cp.n = n;
+  cp.decay = float(1.0 - double(params->lr) * double(params->wd));
+  cp.lr = params->lr;
+  cp.mu = params->mu;
+  cp.eps = params->eps;
+  cp.partials = static_cast<float*>(ws);
+  int64_t rows = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const mo_matrix& t = shards[i];
+    mo::RmnpEntry& E = cp.e[i];
+    E.W = t.W;
+    E.G = static_cast<const uint16_t*>(t.G);
+    E.V = t.V;
+    E.R = int32_t(t.rows);
+    E.C = int32_t(t.cols);
+    E.scale = scales[i];
+    E.vec_ok = (t.cols % 4 == 0) ? 1 : 0;
+    cp.row_prefix[i] = rows;
+    rows += t.rows;
+    int32_t a = i, b = i;
+    while (a > 0 && group[a - 1] == group[i]) --a;
+    while (b + 1 < n && group[b + 1] == group[i]) ++b;
+    cp.first[i] = int16_t(a);
+    cp.last[i] = int16_t(b);
+  }
+  cp.row_prefix[n] = rows;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, int64_t(dev->sms) * 8)));
+  cudaError_t e = mo::launch_rmnp_colcut(cp, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MO_OK;
+}
+
 int adamw_tail_step(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* params, cudaStream_t stream) {
   int st = mo::validate_adamw(segs, n, params);
   if (st != MO_OK) return st;

@@ -335,6 +335,96 @@ __global__ void __launch_bounds__(256) rmnp_kernel(const __grid_constant__ RmnpP
   }
 }
 
+// ------------------------------------------------------------------ column-cut RMNP
+//
+// Rows cut into column shards ("Optimizers In A Sharded World", section 3):
+// pass 1 updates each shard's momentum and writes one fp32 sum of squares per
+// shard row; pass 2 adds, for every row, the partials of all shards of its
+// matrix in table order (in place of the page's all-reduce), clamps the
+// square root at eps and applies the update to the shard. Warp per row, as
+// rmnp_kernel.
+
+__device__ __forceinline__ int colcut_entry(const ColcutParams& p, int64_t row) {
+  int lo = 0, hi = p.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.row_prefix[mid] <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(256) colcut_partial_kernel(const __grid_constant__ ColcutParams p) {
+  const int lane = int(threadIdx.x & 31);
+  const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t total = p.row_prefix[p.n];
+  for (int64_t row = gw; row < total; row += nw) {
+    const int ei = colcut_entry(p, row);
+    const RmnpEntry& E = p.e[ei];
+    const int C = E.C;
+    const size_t off = size_t(row - p.row_prefix[ei]) * size_t(C);
+    float* __restrict__ Vr = E.V + off;
+    const uint16_t* __restrict__ Gr = E.G + off;
+    float ss = 0.f;
+    if (E.vec_ok) {
+      for (int cc = lane * 4; cc < C; cc += 128) {
+        const float4 v = *reinterpret_cast<const float4*>(Vr + cc);
+        const uint2 g = *reinterpret_cast<const uint2*>(Gr + cc);
+        float4 n4;
+        n4.x = fmaf(p.mu, v.x, bf16_bits_to_float(g.x & 0xFFFFu));
+        n4.y = fmaf(p.mu, v.y, bf16_bits_to_float(g.x >> 16));
+        n4.z = fmaf(p.mu, v.z, bf16_bits_to_float(g.y & 0xFFFFu));
+        n4.w = fmaf(p.mu, v.w, bf16_bits_to_float(g.y >> 16));
+        *reinterpret_cast<float4*>(Vr + cc) = n4;
+        ss = fmaf(n4.x, n4.x, ss);
+        ss = fmaf(n4.y, n4.y, ss);
+        ss = fmaf(n4.z, n4.z, ss);
+        ss = fmaf(n4.w, n4.w, ss);
+      }
+    } else {
+      for (int cc = lane; cc < C; cc += 32) {
+        const float vn = fmaf(p.mu, Vr[cc], bf16_bits_to_float(Gr[cc]));
+        Vr[cc] = vn;
+        ss = fmaf(vn, vn, ss);
+      }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) p.partials[row] = ss;
+  }
+}
+
+__global__ void __launch_bounds__(256) colcut_apply_kernel(const __grid_constant__ ColcutParams p) {
+  const int lane = int(threadIdx.x & 31);
+  const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t total = p.row_prefix[p.n];
+  for (int64_t row = gw; row < total; row += nw) {
+    const int ei = colcut_entry(p, row);
+    const RmnpEntry& E = p.e[ei];
+    const int64_t r = row - p.row_prefix[ei];
+    float sum = 0.f;
+    for (int s = p.first[ei]; s <= p.last[ei]; ++s) sum += p.partials[p.row_prefix[s] + r];
+    const float k = p.lr * E.scale / fmaxf(sqrtf(sum), p.eps);
+    const int C = E.C;
+    const size_t off = size_t(r) * size_t(C);
+    const float* __restrict__ Vr = E.V + off;
+    float* __restrict__ Wr = E.W + off;
+    if (E.vec_ok) {
+      for (int cc = lane * 4; cc < C; cc += 128) {
+        const float4 v = *reinterpret_cast<const float4*>(Vr + cc);
+        float4 w = *reinterpret_cast<const float4*>(Wr + cc);
+        w.x = w.x * p.decay - k * v.x;
+        w.y = w.y * p.decay - k * v.y;
+        w.z = w.z * p.decay - k * v.z;
+        w.w = w.w * p.decay - k * v.w;
+        *reinterpret_cast<float4*>(Wr + cc) = w;
+      }
+    } else {
+      for (int cc = lane; cc < C; cc += 32) Wr[cc] = Wr[cc] * p.decay - k * Vr[cc];
+    }
+  }
+}
+
 // ------------------------------------------------------------------ AdamW
 //
 // Decoupled AdamW with bias correction on the packed tail ("MatrixFSDP",
@@ -416,6 +506,15 @@ cudaError_t launch_muon_prologue(const ProParams& p, int max_grid, cudaStream_t 
 cudaError_t launch_rmnp(const RmnpParams& p, int grid, cudaStream_t stream) {
   if (p.n <= 0 || p.row_prefix[p.n] <= 0) return cudaSuccess;
   rmnp_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmnp_colcut(const ColcutParams& p, int grid, cudaStream_t stream) {
+  if (p.n <= 0 || p.row_prefix[p.n] <= 0) return cudaSuccess;
+  colcut_partial_kernel<<<grid, 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  colcut_apply_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

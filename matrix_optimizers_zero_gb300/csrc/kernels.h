@@ -69,6 +69,18 @@ struct RmnpParams {
 };
 cudaError_t launch_rmnp(const RmnpParams& p, int grid, cudaStream_t stream);
 
+// ---------------------------------------------------------------- column-cut RMNP
+struct ColcutParams {
+  RmnpEntry e[kRmnpMaxEntries];
+  int64_t row_prefix[kRmnpMaxEntries + 1];   // prefix sums of shard rows (= partial offsets)
+  int16_t first[kRmnpMaxEntries];            // first and last entry of each entry's group
+  int16_t last[kRmnpMaxEntries];
+  float* partials;
+  int32_t n;
+  float decay, lr, mu, eps;
+};
+cudaError_t launch_rmnp_colcut(const ColcutParams& p, int grid, cudaStream_t stream);
+
 // ---------------------------------------------------------------- AdamW
 constexpr int kAdamMaxSegs = 256;
 constexpr int kAdamItem = 4096;   // elements per work item (1024 float4)

@@ -203,6 +203,36 @@ def rmnp_row_sharded(V: np.ndarray, shards: int, eps: float = RMNP_EPS) -> np.nd
     return np.concatenate(parts, axis=0)
 
 
+RMNP_COLCUT_EPS = 1e-7   # clamp of the column-cut scheme ([SHARD] appendix)
+
+
+def rmnp_colcut_direction(V_shards: Sequence[np.ndarray], eps: float = RMNP_COLCUT_EPS) -> List[np.ndarray]:
+    """RMNP when each row is cut into column shards ([SHARD] section 3,
+    column-cut tensor parallelism; appendix rmnp_colcut): every shard
+    contributes the sum of squares of its part of each row, the per-row
+    partial sums are added over the shards (the page's all-reduce), and each
+    shard divides its part by max(sqrt(total), eps)."""
+    shards = [np.asarray(v, np.float64) for v in V_shards]
+    total = np.zeros(shards[0].shape[0])
+    for v in shards:
+        total = total + np.sum(v * v, axis=1)
+    norm = np.maximum(np.sqrt(total), eps)
+    return [v / norm[:, None] for v in shards]
+
+
+def rmnp_colcut_matrix_step(W_shards, G_shards, V_shards, rows: int, cols: int, lr=0.02, wd=0.01, mu=0.95,
+                            eps=RMNP_COLCUT_EPS):
+    """Column-cut RMNP step over the shards of one [rows, cols] matrix:
+    momentum per shard, the cut-row normalisation above, and the same
+    shape-scaled decoupled update as unsharded RMNP (scale of the whole
+    matrix). Returns (W_new_shards, V_new_shards, D_shards)."""
+    Vn = [momentum(V, G, mu) for V, G in zip(V_shards, G_shards)]
+    D = rmnp_colcut_direction(Vn, eps)
+    s = shape_scale(rows, cols)
+    Wn = [decoupled_update(W, d, lr, wd, s) for W, d in zip(W_shards, D)]
+    return Wn, Vn, D
+
+
 # ---------------------------------------------------------------------------
 # AdamW on the packed non-matrix tail ([MFSDP] sections 3, 4.4, 5.1)
 # ---------------------------------------------------------------------------

@@ -147,3 +147,62 @@ def test_adamw_update_direction_exposed():
 
 def test_adamw_more_than_one_launch_of_segments():
     adam_check([17] * 300, steps=1)
+
+
+# ---------------------------------------------------------------- column-cut RMNP
+
+def _cut(t, widths):
+    out, c = [], 0
+    for w in widths:
+        out.append(t[:, c:c + w].contiguous())
+        c += w
+    return out
+
+
+def test_rmnp_colcut_parity_and_equivalence():
+    """Rows cut into column shards (the page's column-cut layout: 8 shards of
+    a 3840 x 1280 qkv-shaped matrix, plus an uneven 2-way cut): each shard
+    matches the oracle's column-cut step, and reassembled they match the
+    unsharded RMNP step within fp32 reassociation."""
+    p = mo.RmnpParams(lr=0.02, wd=0.01, mu=0.95, eps=1e-7)
+    specs = [((3840, 1280), [160] * 8), ((64, 128), [100, 28]), ((33, 257), [257])]
+    shards, groups, scales, refs = [], [], [], []
+    for gi, ((R, C), widths) in enumerate(specs):
+        wl = workloads.custom_workload([(R, C)], g_std=1e-3, config_id=70 + gi)
+        W, G, V = workloads.host_matrix(wl, 0, v_std=1e-3)
+        Ws, Gs, Vs = _cut(W, widths), _cut(G, widths), _cut(V, widths)
+        for w, g, v in zip(Ws, Gs, Vs):
+            shards.append((w.to(DEV), g.to(DEV), v.to(DEV)))
+            groups.append(gi)
+            scales.append(shape_scale(R, C))
+        refs.append(((R, C), widths, oracle.rmnp_colcut_matrix_step(
+            [f64(w) for w in Ws], [f64(g) for g in Gs], [f64(v) for v in Vs], R, C, lr=p.lr, wd=p.wd, mu=p.mu,
+            eps=p.eps), (W, G, V)))
+    mo.rmnp_colcut_step(shards, groups, scales, p)
+    torch.cuda.synchronize()
+    k = 0
+    for (R, C), widths, (Wn, Vn, _), (W, G, V) in refs:
+        got_w, got_v = [], []
+        for j in range(len(widths)):
+            assert max_rel(f64(shards[k][0]), Wn[j]) <= FP32_MAX_REL_TOL
+            assert max_rel(f64(shards[k][2]), Vn[j]) <= FP32_MAX_REL_TOL
+            got_w.append(f64(shards[k][0]))
+            got_v.append(f64(shards[k][2]))
+            k += 1
+        # reassembled: the unsharded RMNP step on the whole matrix
+        Wd, Gd, Vd = W.to(DEV), G.to(DEV), V.to(DEV)
+        mo.rmnp_step([(Wd, Gd, Vd)], mo.RmnpParams(lr=p.lr, wd=p.wd, mu=p.mu))
+        torch.cuda.synchronize()
+        assert max_rel(np.concatenate(got_w, axis=1), f64(Wd)) <= FP32_MAX_REL_TOL
+        assert max_rel(np.concatenate(got_v, axis=1), f64(Vd)) <= FP32_MAX_REL_TOL
+
+
+def test_rmnp_colcut_validation():
+    W = torch.zeros(8, 16, device=DEV)
+    G = torch.zeros(8, 16, device=DEV, dtype=torch.bfloat16)
+    V = torch.zeros(8, 16, device=DEV)
+    W2, G2, V2 = W.clone(), G.clone(), V.clone()
+    with pytest.raises(mo.MoError):      # a group split across the table
+        mo.rmnp_colcut_step([(W, G, V), (W2, G2, V2), (W.clone(), G.clone(), V.clone())], [0, 1, 0], [1, 1, 1])
+    with pytest.raises(mo.MoError):      # shards of one matrix with different rows
+        mo.rmnp_colcut_step([(W, G, V), (W2[:4], G2[:4], V2[:4])], [0, 0], [1, 1])

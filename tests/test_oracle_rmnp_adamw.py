@@ -106,3 +106,21 @@ def test_adamw_closed_forms():
         np.testing.assert_allclose(p, prev * (1 - lr * wd) - lr * g / (np.abs(g) + eps), rtol=1e-12)
     with pytest.raises(ValueError):
         adamw_step(p, g, m, v, step=0)
+
+
+def test_colcut_rmnp_equals_unsharded_rows():
+    """Cutting every row into column shards and adding the per-row partial
+    sums gives the same row norms (the page: a row's squared norm is the sum
+    of its shards' squared norms); only the clamp differs (1e-7)."""
+    from oracle import rmnp_colcut_direction
+    rng = np.random.default_rng(12)
+    V = rng.standard_normal((40, 384)) * rng.uniform(0.1, 3, size=(40, 1))
+    for cuts in ([384], [160] * 2 + [64], [48] * 8, [1, 383]):
+        edges = np.cumsum([0] + cuts)
+        shards = [V[:, a:b] for a, b in zip(edges[:-1], edges[1:])]
+        D = np.concatenate(rmnp_colcut_direction(shards), axis=1)
+        np.testing.assert_allclose(D, rmnp_direction(V), rtol=1e-14, atol=0)
+    Z = np.zeros((3, 10))
+    Z[1, 4] = 1e-9        # norm below the column-cut clamp
+    D = np.concatenate(rmnp_colcut_direction([Z[:, :6], Z[:, 6:]]), axis=1)
+    assert np.all(D[0] == 0) and D[1, 4] == pytest.approx(1e-9 / 1e-7, rel=1e-15)
