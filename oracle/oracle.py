@@ -25,7 +25,11 @@ Sources (cited by page title and section):
 Readings where the pages are silent (each also listed in the design notes):
   * The iteration is written as A = X X^T, B = b A + c A A, X' = a X + B X.
     The appendix script writes it as A = X X^T, B = A X, X' = a X + b B + c A B;
-    the two are equal in exact arithmetic (a self-check pins this).
+    the two are equal in exact arithmetic (a self-check pins this). The
+    appendix form is kept as a selectable variant.
+  * Nesterov momentum (torch.optim.Muon's default, used by [MFSDP] section
+    5.1) is an option, off by default: the appendix script updates with the
+    plain momentum.
   * The Frobenius norm is taken of the fp32 momentum; X0 = bf16(V / (||V|| + eps)).
   * Weight decay is decoupled and multiplicative for Muon and RMNP, with the
     same learning rate: W <- W (1 - lr wd) - lr s D.
@@ -129,19 +133,32 @@ def newton_schulz(X0: np.ndarray, coeffs: Sequence[float] = NS_COEFFS, steps: in
 
 
 def newton_schulz_pages_form(X0: np.ndarray, coeffs: Sequence[float] = NS_COEFFS,
-                             steps: int = 5) -> np.ndarray:
-    """The same iteration in the algebraic form of the appendix script:
-    A = X X^T, B = A X, X' = a X + b B + c A B (no rounding). Used only to
-    check that the two forms agree."""
+                             steps: int = 5, round_bf16: bool = False,
+                             trace: Optional[list] = None) -> np.ndarray:
+    """The same iteration in the algebraic form of the appendix script
+    ([SHARD] appendix "The Code That Ran", the quintic iteration):
+        A  = X X^T
+        B  = A X            (m x n, unlike the m x m B of newton_schulz)
+        X' = a X + b B + c A B
+    With round_bf16, X (before every iteration), A and B are rounded to bf16
+    (the matrices the GPU stores between products); a X + b B + c A B is
+    combined unrounded and the final iterate is returned unrounded."""
     a, b, c = (float(t) for t in coeffs)
+    q = bf16_round if round_bf16 else _identity
     X = np.asarray(X0, np.float64)
     tall = X.shape[0] > X.shape[1]
     if tall:
         X = X.T
-    for _ in range(steps):
-        A = X @ X.T
-        B = A @ X
-        X = a * X + b * B + c * (A @ B)
+    X = q(X)
+    if trace is not None:
+        trace.append(("X0", X))
+    for k in range(steps):
+        A = q(X @ X.T)
+        B = q(A @ X)
+        Xn = a * X + b * B + c * (A @ B)
+        X = q(Xn) if k < steps - 1 else Xn
+        if trace is not None:
+            trace.extend([(f"A{k}", A), (f"B{k}", B), (f"X{k + 1}", X)])
     return X.T if tall else X
 
 
@@ -151,6 +168,23 @@ def shape_scale(rows: int, cols: int) -> float:
     return math.sqrt(max(1.0, rows / cols))
 
 
+def match_rms_adamw_scale(rows: int, cols: int) -> float:
+    """0.2 sqrt(max(rows, cols)): the learning-rate adjustment named
+    match_rms_adamw in the convergence settings of [MFSDP] section 5.1, as
+    torch.optim.Muon (which that section uses) defines it: it brings the RMS
+    of the orthogonalised update to that of a typical AdamW update."""
+    return 0.2 * math.sqrt(max(rows, cols))
+
+
+def nesterov_direction(V_new: np.ndarray, G: np.ndarray, mu: float) -> np.ndarray:
+    """Nesterov look-ahead G_t + mu V_t. [MFSDP] section 5.1 runs
+    torch.optim.Muon, whose default update is the Nesterov one; with the
+    momentum written V_t = mu V_{t-1} + G_t ([SHARD] section 1) that update is
+    (1 - mu)(G_t + mu V_t), and the positive factor cancels in the Frobenius
+    normalisation (up to eps)."""
+    return np.asarray(G, np.float64) + mu * np.asarray(V_new, np.float64)
+
+
 def decoupled_update(W: np.ndarray, D: np.ndarray, lr: float, wd: float, scale: float) -> np.ndarray:
     """W <- W (1 - lr wd) - lr scale D (decoupled weight decay, [MFSDP]
     section 5.1 gives wd; the multiplicative form is the reading taken)."""
@@ -158,16 +192,34 @@ def decoupled_update(W: np.ndarray, D: np.ndarray, lr: float, wd: float, scale: 
 
 
 def muon_matrix_step(W, G, V, lr=0.02, wd=0.01, mu=0.95, coeffs=NS_COEFFS, eps=NS_EPS,
-                     ns_steps=5, round_bf16=True):
+                     ns_steps=5, round_bf16=True, nesterov=False, lr_adjust="original",
+                     ns_form="gram"):
     """One owner-local Muon step on a whole 2D matrix ([MFSDP] section 3: the
     owner holds the full gradient; [SHARD] section 1 and appendix for the
     arithmetic). Returns (W_new, V_new, O) where O is the Newton-Schulz output
-    in the stored orientation."""
+    in the stored orientation.
+
+    Variants: nesterov=True orthogonalises G + mu V_new instead of V_new;
+    lr_adjust="match_rms_adamw" replaces the shape scale by
+    0.2 sqrt(max(rows, cols)); ns_form="appendix" runs the iteration in the
+    appendix script's algebraic form (newton_schulz_pages_form)."""
     R, C = np.shape(W)
     Vn = momentum(V, G, mu)
-    X0 = frobenius_normalize(Vn, eps)
-    O = newton_schulz(X0, coeffs, ns_steps, round_bf16=round_bf16)
-    Wn = decoupled_update(W, O, lr, wd, shape_scale(R, C))
+    U = nesterov_direction(Vn, G, mu) if nesterov else Vn
+    X0 = frobenius_normalize(U, eps)
+    if ns_form == "gram":
+        O = newton_schulz(X0, coeffs, ns_steps, round_bf16=round_bf16)
+    elif ns_form == "appendix":
+        O = newton_schulz_pages_form(X0, coeffs, ns_steps, round_bf16=round_bf16)
+    else:
+        raise ValueError(f"unknown ns_form {ns_form!r}")
+    if lr_adjust == "original":
+        scale = shape_scale(R, C)
+    elif lr_adjust == "match_rms_adamw":
+        scale = match_rms_adamw_scale(R, C)
+    else:
+        raise ValueError(f"unknown lr_adjust {lr_adjust!r}")
+    Wn = decoupled_update(W, O, lr, wd, scale)
     return Wn, Vn, O
 
 
