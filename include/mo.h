@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define MO_ABI_VERSION 1
+#define MO_ABI_VERSION 2
 
 enum mo_status {
   MO_OK = 0,
@@ -68,14 +68,31 @@ typedef struct {
 
 /* Muon hyperparameters ("Optimizers In A Sharded World", section 1 and the
  * appendix benchmark script; "MatrixFSDP", section 5.1 for weight decay).
- *   V <- mu V + G;  X0 = V / (||V||_F + eps), transposed if rows > cols;
- *   ns_steps x { A = X X^T;  B = b A + c A A;  X = a X + B X };
- *   W <- W (1 - lr wd) - lr sqrt(max(1, rows/cols)) X (transposed back).
+ *   V <- mu V + G;  U = V (or G + mu V with nesterov);
+ *   X0 = U / (||U||_F + eps), transposed if rows > cols;
+ *   ns_steps x { A = X X^T;  B = b A + c A A;  X = a X + B X }   (MO_NS_GRAM)
+ *   ns_steps x { A = X X^T;  B = A X;  X = a X + b B + c A B }   (MO_NS_APPENDIX)
+ *   W <- W (1 - lr wd) - lr s X (transposed back), with
+ *   s = sqrt(max(1, rows/cols)) (MO_LR_ORIGINAL) or 0.2 sqrt(max(rows, cols))
+ *   (MO_LR_MATCH_RMS_ADAMW).
  * Defaults: lr 0.02, wd 0.01, mu 0.95, (a,b,c) = (3.4445, -4.7750, 2.0315),
- * eps 1e-7, ns_steps 5. ns_steps must be in [1, 100]. */
+ * eps 1e-7, ns_steps 5, ns_form MO_NS_GRAM, lr_adjust MO_LR_ORIGINAL,
+ * nesterov 0. ns_steps must be in [1, 100]; nesterov 0 or 1.
+ *  - MO_NS_GRAM is the fast form (5 (3 m^2 n + m^3) flops for m <= n). The
+ *    appendix script's form costs 25 m^2 n and needs a larger workspace
+ *    (mo_muon_workspace_bytes depends on ns_form); the two agree in exact
+ *    arithmetic and differ by bf16 rounding.
+ *  - nesterov and MO_LR_MATCH_RMS_ADAMW are the update of torch.optim.Muon,
+ *    which "MatrixFSDP" section 5.1 runs (with match_rms_adamw, momentum 0.5
+ *    and 2 Newton-Schulz steps for its convergence runs). */
+enum mo_ns_form { MO_NS_GRAM = 0, MO_NS_APPENDIX = 1 };
+enum mo_lr_adjust { MO_LR_ORIGINAL = 0, MO_LR_MATCH_RMS_ADAMW = 1 };
 typedef struct {
   float lr, wd, mu, a, b, c, eps;
   int32_t ns_steps;
+  int32_t ns_form;     /* enum mo_ns_form */
+  int32_t lr_adjust;   /* enum mo_lr_adjust */
+  int32_t nesterov;    /* 0: orthogonalise V; 1: orthogonalise G + mu V */
 } mo_muon_params;
 
 /* RMNP hyperparameters ("Optimizers In A Sharded World", section 1 and the
@@ -115,8 +132,9 @@ size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_pa
  * call (two calls in flight on different streams must not share it).
  * Launches: one fused momentum + norm + bf16-cast prologue, then for each of
  * the ns_steps iterations three grouped tcgen05 GEMM launches (Gram, A.A with
- * the b A + c A A epilogue, B.X with the a X + epilogue); the last B.X launch
- * applies the weight update in its epilogue. Matrices are independent. */
+ * the b A + c A A epilogue, B.X with the a X + epilogue; with MO_NS_APPENDIX:
+ * Gram, A.X, A.B with the a X + b B + epilogue); the last launch applies the
+ * weight update in its epilogue. Matrices are independent. */
 int muon_owner_step(const mo_matrix* tbl, int32_t n, const mo_muon_params* params,
                     void* ws, size_t ws_bytes, cudaStream_t stream);
 

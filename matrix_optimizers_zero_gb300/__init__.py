@@ -33,13 +33,23 @@ class MoMatrix(ctypes.Structure):
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
 
 
+NS_FORMS = {"gram": 0, "appendix": 1}                  # mo_ns_form
+LR_ADJUST = {"original": 0, "match_rms_adamw": 1}      # mo_lr_adjust
+
+
 class MuonParams(ctypes.Structure):
+    """mo_muon_params. ns_form and lr_adjust take the names of NS_FORMS and
+    LR_ADJUST (or their integer codes)."""
     _fields_ = [("lr", ctypes.c_float), ("wd", ctypes.c_float), ("mu", ctypes.c_float),
                 ("a", ctypes.c_float), ("b", ctypes.c_float), ("c", ctypes.c_float),
-                ("eps", ctypes.c_float), ("ns_steps", ctypes.c_int32)]
+                ("eps", ctypes.c_float), ("ns_steps", ctypes.c_int32), ("ns_form", ctypes.c_int32),
+                ("lr_adjust", ctypes.c_int32), ("nesterov", ctypes.c_int32)]
 
-    def __init__(self, lr=0.02, wd=0.01, mu=0.95, a=3.4445, b=-4.7750, c=2.0315, eps=1e-7, ns_steps=5):
-        super().__init__(lr, wd, mu, a, b, c, eps, ns_steps)
+    def __init__(self, lr=0.02, wd=0.01, mu=0.95, a=3.4445, b=-4.7750, c=2.0315, eps=1e-7, ns_steps=5,
+                 ns_form="gram", lr_adjust="original", nesterov=False):
+        form = NS_FORMS[ns_form] if isinstance(ns_form, str) else int(ns_form)
+        adj = LR_ADJUST[lr_adjust] if isinstance(lr_adjust, str) else int(lr_adjust)
+        super().__init__(lr, wd, mu, a, b, c, eps, ns_steps, form, adj, int(nesterov))
 
 
 class RmnpParams(ctypes.Structure):

@@ -86,8 +86,9 @@ std::mutex g_plan_mu;
 std::vector<PlanEntry*> g_plans;
 uint64_t g_plan_clock = 0;
 
-bool same_table(const PlanEntry& e, int dev, const mo_matrix* tbl, int32_t n, const void* ws) {
-  return e.dev == dev && e.ws == reinterpret_cast<uintptr_t>(ws) && e.table.size() == size_t(n) &&
+bool same_table(const PlanEntry& e, int dev, const mo_matrix* tbl, int32_t n, int ns_form, const void* ws) {
+  return e.dev == dev && e.ws == reinterpret_cast<uintptr_t>(ws) && e.L.ns_form == ns_form &&
+         e.table.size() == size_t(n) &&
          std::memcmp(e.table.data(), tbl, sizeof(mo_matrix) * size_t(n)) == 0;
 }
 
@@ -111,7 +112,7 @@ int build_entry(PlanEntry& E, const mo_matrix* tbl, int32_t n, void* ws) {
     d.X[1] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[1]));
     d.A = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.A));
     d.B = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.B));
-    if (!mo::encode_matrix_maps(d, E.header.data() + L.off_tmaps + size_t(i) * mo::kMapsPerMat * mo::kTensorMapBytes))
+    if (!mo::encode_matrix_maps(d, L.ns_form, E.header.data() + L.off_tmaps + size_t(i) * mo::kMapsPerMat * mo::kTensorMapBytes))
       return cuda_fail(cudaErrorInvalidValue);
   }
   std::memcpy(E.header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * size_t(n));
@@ -125,9 +126,9 @@ int build_entry(PlanEntry& E, const mo_matrix* tbl, int32_t n, void* ws) {
   return MO_OK;
 }
 
-PlanEntry* find_plan(int dev, const mo_matrix* tbl, int32_t n, const void* ws) {
+PlanEntry* find_plan(int dev, const mo_matrix* tbl, int32_t n, int ns_form, const void* ws) {
   for (PlanEntry* e : g_plans)
-    if ((dev < 0 || e->dev == dev) && same_table(*e, e->dev, tbl, n, ws)) return e;
+    if ((dev < 0 || e->dev == dev) && same_table(*e, e->dev, tbl, n, ns_form, ws)) return e;
   return nullptr;
 }
 
@@ -180,11 +181,11 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
 
   std::lock_guard<std::mutex> lock(g_plan_mu);
   // Host-only part first: a rejected call makes no CUDA call.
-  PlanEntry* E = find_plan(-1, tbl, n, ws);
+  PlanEntry* E = find_plan(-1, tbl, n, prm->ns_form, ws);
   PlanEntry* fresh = nullptr;
   if (E == nullptr) {
     fresh = new PlanEntry();
-    mo::plan_muon(tbl, n, mo::kBM, fresh->L);
+    mo::plan_muon(tbl, n, mo::kBM, prm->ns_form, fresh->L);
   }
   const size_t need = (E ? E->L : fresh->L).total_bytes;
   if (ws_bytes < need) {
@@ -199,10 +200,10 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   }
   if (E != nullptr && E->dev != dev_id) {
     // same addresses on another device: look for that device's entry
-    E = find_plan(dev_id, tbl, n, ws);
+    E = find_plan(dev_id, tbl, n, prm->ns_form, ws);
     if (E == nullptr) {
       fresh = new PlanEntry();
-      mo::plan_muon(tbl, n, mo::kBM, fresh->L);
+      mo::plan_muon(tbl, n, mo::kBM, prm->ns_form, fresh->L);
     }
   }
   if (E == nullptr) {
@@ -239,6 +240,7 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   pp.total_items = L.seg_prefix.back();
   pp.mu = prm->mu;
   pp.eps = prm->eps;
+  pp.nesterov = prm->nesterov;
   pp.timeout_ns = 2000000000ull;
   if ((e = mo::launch_muon_prologue(pp, 0, stream)) != cudaSuccess) return cuda_fail(e);
   if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) return cuda_fail(e);
@@ -252,16 +254,22 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   np.c = prm->c;
   np.lr = prm->lr;
   np.decay = float(1.0 - double(prm->lr) * double(prm->wd));
+  np.lr_adjust = prm->lr_adjust;
   np.timeout_ns = 2000000000ull;
+  // Launch kinds of one iteration and the tile schedule each one uses.
+  const bool appendix = prm->ns_form == MO_NS_APPENDIX;
+  const int kinds[3] = {MO_PHASE_GRAM, appendix ? mo::kPhaseAX : MO_PHASE_POLY,
+                        appendix ? mo::kPhaseABX : MO_PHASE_UPDATE};
+  const int sched[3] = {MO_PHASE_GRAM, appendix ? MO_PHASE_UPDATE : MO_PHASE_POLY, MO_PHASE_UPDATE};
   int cur = 0;
   for (int it = 0; it < prm->ns_steps; ++it) {
     np.cur = cur;
-    for (int ph = 0; ph < 3; ++ph) {
-      np.tiles = reinterpret_cast<const mo::TileRec*>(wsb + L.off_tiles[ph]);
-      np.ntiles = int32_t(L.tiles[ph].size());
-      const bool last = (ph == MO_PHASE_UPDATE) && (it == prm->ns_steps - 1);
+    for (int k = 0; k < 3; ++k) {
+      np.tiles = reinterpret_cast<const mo::TileRec*>(wsb + L.off_tiles[sched[k]]);
+      np.ntiles = int32_t(L.tiles[sched[k]].size());
+      const bool last = (k == 2) && (it == prm->ns_steps - 1);
       const int grid = 2 * std::max(1, std::min(np.ntiles, dev->sms / 2));
-      if ((e = mo::launch_ns_phase(ph, last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
+      if ((e = mo::launch_ns_phase(kinds[k], last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
     }
     cur ^= 1;
   }
@@ -329,7 +337,7 @@ size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_pa
   if (mo::validate_matrix_table(tbl, n) != MO_OK) return 0;
   if (n == 0) return 0;
   mo::MuonLayout L;
-  mo::plan_muon(tbl, n, mo::kBM, L);
+  mo::plan_muon(tbl, n, mo::kBM, params->ns_form, L);
   return L.total_bytes;
 }
 

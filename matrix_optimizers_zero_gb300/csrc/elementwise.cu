@@ -25,13 +25,16 @@ __device__ __forceinline__ float warp_sum(float x) {
 //
 // One persistent cooperative launch over a work list of two item kinds:
 //   norm items   momentum V <- mu V + G ("Optimizers In A Sharded World",
-//                section 1) over a flat 8192-element chunk of a stored
-//                matrix, with one fp32 sum of squares per chunk. The CTA that
-//                completes a matrix's last chunk sums that matrix's partials
-//                in a fixed order (deterministic, no float atomics), writes
-//                the Frobenius scale 1 / (||V|| + eps) (eps added to the norm,
-//                as in the same page's appendix) and marks the matrix ready.
-//   cast items   X0 = bf16(V * scale) for a 64 x 128 tile, written in the wide
+//                section 1) over a flat 32768-element chunk of a stored
+//                matrix, with one fp32 sum of squares of U per chunk, where
+//                U = V, or U = G + mu V with Nesterov momentum (the default
+//                update of torch.optim.Muon, which "MatrixFSDP" section 5.1
+//                runs). The CTA that completes a matrix's last chunk sums
+//                that matrix's partials in a fixed order (deterministic, no
+//                float atomics), writes the Frobenius scale 1 / (||U|| + eps)
+//                (eps added to the norm, as in the same page's appendix) and
+//                marks the matrix ready.
+//   cast items   X0 = bf16(U * scale) for a 64 x 128 tile, written in the wide
 //                orientation (transposed through shared memory when
 //                rows > cols, appendix of the same page).
 // The list interleaves matrices (norm 0, norm 1, cast 0, norm 2, cast 1, ...)
@@ -45,6 +48,7 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
+template <bool NEST>
 __device__ void prologue_norm_item(const ProParams& p, int mi, int64_t local, float* red, int* last_flag) {
   const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
   const DevMat& M = p.mats[mi];
@@ -70,21 +74,32 @@ __device__ void prologue_norm_item(const ProParams& p, int mi, int64_t local, fl
     for (int j = 0; j < 8; ++j) {
       const int e = base + (j * 256 + tid) * 4;
       if (e + 4 <= cnt) {
+        const float g0 = bf16_bits_to_float(g[j].x & 0xFFFFu), g1 = bf16_bits_to_float(g[j].x >> 16);
+        const float g2 = bf16_bits_to_float(g[j].y & 0xFFFFu), g3 = bf16_bits_to_float(g[j].y >> 16);
         float4 n4;
-        n4.x = fmaf(p.mu, v[j].x, bf16_bits_to_float(g[j].x & 0xFFFFu));
-        n4.y = fmaf(p.mu, v[j].y, bf16_bits_to_float(g[j].x >> 16));
-        n4.z = fmaf(p.mu, v[j].z, bf16_bits_to_float(g[j].y & 0xFFFFu));
-        n4.w = fmaf(p.mu, v[j].w, bf16_bits_to_float(g[j].y >> 16));
+        n4.x = fmaf(p.mu, v[j].x, g0);
+        n4.y = fmaf(p.mu, v[j].y, g1);
+        n4.z = fmaf(p.mu, v[j].z, g2);
+        n4.w = fmaf(p.mu, v[j].w, g3);
         *reinterpret_cast<float4*>(V + e) = n4;
-        ss = fmaf(n4.x, n4.x, ss);
-        ss = fmaf(n4.y, n4.y, ss);
-        ss = fmaf(n4.z, n4.z, ss);
-        ss = fmaf(n4.w, n4.w, ss);
+        float4 u4 = n4;
+        if (NEST) {
+          u4.x = fmaf(p.mu, n4.x, g0);
+          u4.y = fmaf(p.mu, n4.y, g1);
+          u4.z = fmaf(p.mu, n4.z, g2);
+          u4.w = fmaf(p.mu, n4.w, g3);
+        }
+        ss = fmaf(u4.x, u4.x, ss);
+        ss = fmaf(u4.y, u4.y, ss);
+        ss = fmaf(u4.z, u4.z, ss);
+        ss = fmaf(u4.w, u4.w, ss);
       } else {
         for (int k = e; k < cnt && k < e + 4; ++k) {
-          const float vn = fmaf(p.mu, V[k], bf16_bits_to_float(G[k]));
+          const float gk = bf16_bits_to_float(G[k]);
+          const float vn = fmaf(p.mu, V[k], gk);
           V[k] = vn;
-          ss = fmaf(vn, vn, ss);
+          const float u = NEST ? fmaf(p.mu, vn, gk) : vn;
+          ss = fmaf(u, u, ss);
         }
       }
     }
@@ -147,6 +162,27 @@ __device__ bool prologue_wait_ready(const ProParams& p, int mi, int* ok_flag) {
   return *ok_flag != 0;
 }
 
+// U = V, or G + mu V (Nesterov), for four consecutive elements at `off`.
+template <bool NEST>
+__device__ __forceinline__ float4 load_u4(const ProParams& p, const DevMat& M, size_t off) {
+  float4 u = __ldcg(reinterpret_cast<const float4*>(M.V + off));
+  if (NEST) {
+    const uint2 g = *reinterpret_cast<const uint2*>(M.G + off);
+    u.x = fmaf(p.mu, u.x, bf16_bits_to_float(g.x & 0xFFFFu));
+    u.y = fmaf(p.mu, u.y, bf16_bits_to_float(g.x >> 16));
+    u.z = fmaf(p.mu, u.z, bf16_bits_to_float(g.y & 0xFFFFu));
+    u.w = fmaf(p.mu, u.w, bf16_bits_to_float(g.y >> 16));
+  }
+  return u;
+}
+
+template <bool NEST>
+__device__ __forceinline__ float load_u1(const ProParams& p, const DevMat& M, size_t off) {
+  const float v = __ldcg(M.V + off);
+  return NEST ? fmaf(p.mu, v, bf16_bits_to_float(M.G[off])) : v;
+}
+
+template <bool NEST>
 __device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, uint16_t (*tbuf)[kCastTR + 8]) {
   const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
   const DevMat& M = p.mats[mi];
@@ -166,12 +202,12 @@ __device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, ui
       const size_t off = size_t(r) * size_t(C) + size_t(c);
       uint16_t* xp = X + size_t(r) * ldx + size_t(c);
       if (M.vec_ok && c + 4 <= C) {
-        const float4 v4 = __ldcg(reinterpret_cast<const float4*>(M.V + off));
+        const float4 v4 = load_u4<NEST>(p, M, off);
         *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16x2(v4.x * sc, v4.y * sc), pack_bf16x2(v4.z * sc, v4.w * sc));
       } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (c + q < C) xp[q] = float_to_bf16_bits(__ldcg(M.V + off + q) * sc);
+          if (c + q < C) xp[q] = float_to_bf16_bits(load_u1<NEST>(p, M, off + q) * sc);
       }
     }
   } else {
@@ -184,18 +220,32 @@ __device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, ui
     const int r = r0 + rl;
     const int cb = cq * 32;
     if (r < R) {
-      const float* vrow = M.V + size_t(r) * size_t(C) + size_t(c0 + cb);
+      const size_t roff = size_t(r) * size_t(C) + size_t(c0 + cb);
+      const float* vrow = M.V + roff;
       if (c0 + cb + 32 <= C && (reinterpret_cast<uintptr_t>(vrow) & 31u) == 0) {
         uint32_t w8[4][8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) ptx::ld_global_v8_cg(vrow + 8 * j, w8[j]);
+        if (NEST) {
+          // the matching 8 bf16 of G per 32-byte V vector (16-byte aligned)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 g = *reinterpret_cast<const uint4*>(M.G + roff + 8 * j);
+            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float gq = bf16_bits_to_float((q & 1) ? (gw[q >> 1] >> 16) : (gw[q >> 1] & 0xFFFFu));
+              w8[j][q] = __float_as_uint(fmaf(p.mu, __uint_as_float(w8[j][q]), gq));
+            }
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
           for (int q = 0; q < 8; ++q) tbuf[cb + 8 * j + q][rl] = float_to_bf16_bits(__uint_as_float(w8[j][q]) * sc);
       } else {
         for (int j = 0; j < 32; ++j)
-          tbuf[cb + j][rl] = (c0 + cb + j < C) ? float_to_bf16_bits(__ldcg(vrow + j) * sc) : uint16_t(0);
+          tbuf[cb + j][rl] = (c0 + cb + j < C) ? float_to_bf16_bits(load_u1<NEST>(p, M, roff + j) * sc) : uint16_t(0);
       }
     }
     __syncthreads();
@@ -219,6 +269,7 @@ __device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, ui
   }
 }
 
+template <bool NEST>
 __global__ void __launch_bounds__(256, 4) muon_prologue_kernel(const __grid_constant__ ProParams p) {
   __shared__ __align__(16) uint16_t tbuf[kCastTC][kCastTR + 8];
   __shared__ float red[8];
@@ -233,10 +284,10 @@ __global__ void __launch_bounds__(256, 4) muon_prologue_kernel(const __grid_cons
     const int mi = code >> 1;
     const int64_t local = t - p.seg_prefix[lo];
     if ((code & 1) == 0) {
-      prologue_norm_item(p, mi, local, red, &flag);
+      prologue_norm_item<NEST>(p, mi, local, red, &flag);
     } else {
       if (!prologue_wait_ready(p, mi, &flag)) return;   // uniform across the CTA
-      prologue_cast_item(p, mi, local, tbuf);
+      prologue_cast_item<NEST>(p, mi, local, tbuf);
     }
   }
 }
@@ -492,15 +543,15 @@ cudaError_t launch_muon_prologue(const ProParams& p, int max_grid, cudaStream_t 
   cudaError_t e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, muon_prologue_kernel, 256, 0)) != cudaSuccess)
-    return e;
+  const void* kern = p.nesterov ? reinterpret_cast<const void*>(muon_prologue_kernel<true>)
+                                : reinterpret_cast<const void*>(muon_prologue_kernel<false>);
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0)) != cudaSuccess) return e;
   int64_t grid = int64_t(sms) * int64_t(per_sm);
   if (max_grid > 0) grid = std::min<int64_t>(grid, max_grid);
   grid = std::max<int64_t>(1, std::min<int64_t>(grid, p.total_items));
   ProParams copy = p;
   void* args[] = {&copy};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(muon_prologue_kernel), dim3(unsigned(grid)),
-                                     dim3(256), args, 0, stream);
+  return cudaLaunchCooperativeKernel(kern, dim3(unsigned(grid)), dim3(256), args, 0, stream);
 }
 
 cudaError_t launch_rmnp(const RmnpParams& p, int grid, cudaStream_t stream) {

@@ -21,13 +21,17 @@ struct NsParams {
   float a, b, c;
   float lr;
   float decay;                // 1 - lr wd, rounded once from double on the host
+  int32_t lr_adjust;          // mo_lr_adjust: which per-matrix scale the update uses
   uint64_t timeout_ns;
 };
 
-// 256 x 256 tiles on CTA pairs; grid must be even (two CTAs per cluster)
+// 256 x 256 tiles on CTA pairs; grid must be even (two CTAs per cluster).
+// phase: MO_PHASE_GRAM, MO_PHASE_POLY, MO_PHASE_UPDATE, kPhaseAX or kPhaseABX;
+// last (UPDATE and ABX only) applies the weight update in the epilogue.
 cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream);
 size_t ns_gemm_smem_bytes();
-bool encode_matrix_maps(const DevMat& d, void* out_maps);   // writes kMapsPerMat CUtensorMap
+// Writes kMapsPerMat CUtensorMap; with MO_NS_APPENDIX the B buffer is m x n.
+bool encode_matrix_maps(const DevMat& d, int ns_form, void* out_maps);
 cudaError_t device_status_ptr(int** out);
 cudaError_t launch_bounded_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t stream);
 
@@ -40,11 +44,12 @@ struct ProParams {
   uint32_t* counters;         // per matrix, zero on entry, zero again on exit
   uint32_t* ready;            // per matrix, set once its scale is final (zero on entry)
   uint32_t* abort;            // set when any wait of the launch expired (zero on entry)
-  float* scales;              // 1 / (||V_new||_F + eps)
+  float* scales;              // 1 / (||U||_F + eps), U = V_new or G + mu V_new
   int* status;                // device status word
   int32_t nseg;
   int64_t total_items;
   float mu, eps;
+  int32_t nesterov;           // orthogonalise G + mu V_new instead of V_new
   uint64_t timeout_ns;
 };
 // Cooperative launch (all CTAs co-resident): normalise/cast items wait for

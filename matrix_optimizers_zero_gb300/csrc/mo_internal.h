@@ -38,7 +38,7 @@ struct DevMat {
   float* V;                 // [R, C] fp32
   uint16_t* X[2];           // [m, ldx] bf16 ping-pong Newton-Schulz iterates
   uint16_t* A;              // [m, lda] bf16 Gram
-  uint16_t* B;              // [m, lda] bf16 b A + c A A
+  uint16_t* B;              // [m, lda] bf16 b A + c A A; appendix form: [m, ldx] bf16 A X
   int32_t R, C;             // stored shape
   int32_t m, n;             // iteration shape (m <= n)
   int32_t ldx, lda;         // row strides in elements (multiples of 64)
@@ -46,10 +46,16 @@ struct DevMat {
   int32_t vec_ok;           // C % 4 == 0 (16-byte vector access along rows)
   int32_t cast_tiles_c;     // normalise/cast tiles along C
   float shape_scale;        // sqrt(max(1, R/C))
-  int32_t pad0;
+  float rms_scale;          // 0.2 sqrt(max(R, C)) (match_rms_adamw)
   int64_t nrm_base;         // first sum-of-squares chunk (global index)
   int64_t nrm_count;        // sum-of-squares chunks of this matrix
 };
+
+// Newton-Schulz launch kinds beyond the public MO_PHASE_* values: the two
+// m x n products of the appendix form of the iteration, B = A X and
+// X' = a X + b B + c A B. Both use the MO_PHASE_UPDATE tile schedule.
+constexpr int kPhaseAX = 3;
+constexpr int kPhaseABX = 4;
 
 // Identical layout to mo_tile.
 struct TileRec {

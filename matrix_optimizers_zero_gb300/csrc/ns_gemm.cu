@@ -175,32 +175,51 @@ __device__ __forceinline__ void epilogue_symmetric(const NsParams& p, const DevM
 
 // UPDATE: X' = a X + acc (bf16 to the other X buffer), or in the last
 // iteration W <- W decay - lr s X' on the stored orientation.
-template <bool LAST>
+template <int PHASE, bool LAST>
 __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat& M, int row, int cbase,
                                                 uint32_t tb) {
+  // UPDATE: X' = a X + acc.  AX: B = acc.  ABX: X' = a X + b B + c acc.
+  constexpr bool kReadX = PHASE != kPhaseAX;
+  constexpr bool kReadB = PHASE == kPhaseABX;
   const int m = M.m, n = M.n;
   const bool rv = row < m;
-  const uint16_t* x_row = M.X[p.cur] + size_t(rv ? row : 0) * size_t(M.ldx);
-  uint32_t pre[16], nxt[16];
-  prefetch_chunk(x_row, cbase, n, rv, nxt);
+  const size_t roff = size_t(rv ? row : 0) * size_t(M.ldx);
+  const uint16_t* x_row = M.X[p.cur] + roff;
+  const uint16_t* b_row = M.B + roff;
+  uint32_t pre[16], nxt[16], preb[16], nxtb[16];
+  if (kReadX) prefetch_chunk(x_row, cbase, n, rv, nxt);
+  if (kReadB) prefetch_chunk(b_row, cbase, n, rv, nxtb);
 #pragma unroll 1
   for (int ch = 0; ch < kEpiCols / 32; ++ch) {
     const int col0 = cbase + ch * 32;
+    if (kReadX) {
 #pragma unroll
-    for (int q = 0; q < 16; ++q) pre[q] = nxt[q];
-    if (ch + 1 < kEpiCols / 32) prefetch_chunk(x_row, col0 + 32, n, rv, nxt);
+      for (int q = 0; q < 16; ++q) pre[q] = nxt[q];
+      if (ch + 1 < kEpiCols / 32) prefetch_chunk(x_row, col0 + 32, n, rv, nxt);
+    }
+    if (kReadB) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) preb[q] = nxtb[q];
+      if (ch + 1 < kEpiCols / 32) prefetch_chunk(b_row, col0 + 32, n, rv, nxtb);
+    }
     float v[32];
     tmem_chunk(tb + uint32_t(ch * 32), v);
     if (!rv || col0 >= n) continue;
     const bool full = col0 + 32 <= n;
-    {
+    if (kReadB) {
+      float bb[32];
+      chunk_operand(b_row, col0, n, preb, bb);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = fmaf(p.b, bb[i], p.c * v[i]);
+    }
+    if (kReadX) {
       float x[32];
       chunk_operand(x_row, col0, n, pre, x);
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = fmaf(p.a, x[i], v[i]);
     }
     if (!LAST) {
-      uint16_t* o_row = M.X[p.cur ^ 1] + size_t(row) * size_t(M.ldx) + col0;
+      uint16_t* o_row = (PHASE == kPhaseAX ? M.B : M.X[p.cur ^ 1]) + size_t(row) * size_t(M.ldx) + col0;
       if (full) {
         store_bf16x32(o_row, v);
       } else {
@@ -210,7 +229,7 @@ __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat&
       }
     } else {
       const float decay = p.decay;
-      const float step = p.lr * M.shape_scale;
+      const float step = p.lr * (p.lr_adjust == MO_LR_MATCH_RMS_ADAMW ? M.rms_scale : M.shape_scale);
       if (!M.tall) {
         // W is [m, n]: element (row, col)
         float* w_row = M.W + size_t(row) * size_t(M.C) + col0;
@@ -267,6 +286,9 @@ constexpr size_t kPairSmem = 1024 + size_t(kPairStages) * kPairStageBytes + kPai
 
 template <int PHASE, bool LAST>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_constant__ NsParams p) {
+  // m x n outputs (B operand X or A X, MN-major, K = m) vs symmetric m x m ones
+  constexpr bool kWide = PHASE == MO_PHASE_UPDATE || PHASE == kPhaseAX || PHASE == kPhaseABX;
+  static_assert(!LAST || PHASE == MO_PHASE_UPDATE || PHASE == kPhaseABX, "LAST applies to the final product");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -332,9 +354,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
         } else if (PHASE == MO_PHASE_POLY) {
           mapA = mapB = &maps[2];
           K = M.m;
-        } else {
+        } else if (PHASE == MO_PHASE_UPDATE) {
           mapA = &maps[3];
           mapB = &maps[p.cur];
+          K = M.m;
+        } else if (PHASE == kPhaseAX) {
+          mapA = &maps[2];
+          mapB = &maps[p.cur];
+          K = M.m;
+        } else {
+          mapA = &maps[2];
+          mapB = &maps[3];
           K = M.m;
         }
         if (tr.mat != last_mat) {
@@ -358,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
           const int k0 = kb * kBK;
           ptx::tma_load_2d_pair(sa, mapA, fb, k0, arow);
           ptx::tma_load_2d_pair(sa + kBoxBytes, mapA, fb, k0, arow + 64);
-          if (PHASE != MO_PHASE_UPDATE) {
+          if (!kWide) {
             ptx::tma_load_2d_pair(sb, mapB, fb, k0, bcol);
             ptx::tma_load_2d_pair(sb + kBoxBytes, mapB, fb, k0, bcol + 64);
           } else {
@@ -388,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issuer (even CTA)
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, kBN, 0u, PHASE == MO_PHASE_UPDATE ? 1u : 0u);
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, kBN, 0u, kWide ? 1u : 0u);
       int stage = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -414,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = ptx::smem_desc_sw128(sa + uint32_t(kk) * 32u, 16u, 1024u);
-            const uint64_t bd = (PHASE == MO_PHASE_UPDATE)
+            const uint64_t bd = kWide
                                     ? ptx::smem_desc_sw128(sb + uint32_t(kk) * 2048u, kBoxBytes, 1024u)
                                     : ptx::smem_desc_sw128(sb + uint32_t(kk) * 32u, 16u, 1024u);
             ptx::umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
@@ -455,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
       const int cbase = int(tr.tn) * kBN + half * kEpiCols;
       const uint32_t tb = tmem_base + uint32_t(acc) * uint32_t(kBN) + uint32_t(half * kEpiCols) +
                           (uint32_t(quarter * 32) << 16);
-      if (PHASE == MO_PHASE_UPDATE)
-        epilogue_update<LAST>(p, M, row, cbase, tb);
+      if (kWide)
+        epilogue_update<PHASE, LAST>(p, M, row, cbase, tb);
       else
         epilogue_symmetric<PHASE>(p, M, row, cbase, tb);
       ptx::tc_fence_before();
@@ -524,6 +554,10 @@ cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, c
       return launch_pair<MO_PHASE_GRAM, false>(p, grid, stream);
     case MO_PHASE_POLY:
       return launch_pair<MO_PHASE_POLY, false>(p, grid, stream);
+    case kPhaseAX:
+      return launch_pair<kPhaseAX, false>(p, grid, stream);
+    case kPhaseABX:
+      return last ? launch_pair<kPhaseABX, true>(p, grid, stream) : launch_pair<kPhaseABX, false>(p, grid, stream);
     default:
       return last ? launch_pair<MO_PHASE_UPDATE, true>(p, grid, stream)
                   : launch_pair<MO_PHASE_UPDATE, false>(p, grid, stream);
@@ -575,13 +609,15 @@ bool encode_bf16_2d(CUtensorMap* map, void* gaddr, uint64_t cols, uint64_t rows,
 
 }  // namespace
 
-bool encode_matrix_maps(const DevMat& d, void* out_maps) {
+bool encode_matrix_maps(const DevMat& d, int ns_form, void* out_maps) {
   static_assert(sizeof(CUtensorMap) == kTensorMapBytes, "CUtensorMap size");
   CUtensorMap* maps = static_cast<CUtensorMap*>(out_maps);
+  const bool wide_b = ns_form == MO_NS_APPENDIX;   // B = A X is m x n
   return encode_bf16_2d(&maps[0], d.X[0], uint64_t(d.n), uint64_t(d.m), uint64_t(d.ldx)) &&
          encode_bf16_2d(&maps[1], d.X[1], uint64_t(d.n), uint64_t(d.m), uint64_t(d.ldx)) &&
          encode_bf16_2d(&maps[2], d.A, uint64_t(d.m), uint64_t(d.m), uint64_t(d.lda)) &&
-         encode_bf16_2d(&maps[3], d.B, uint64_t(d.m), uint64_t(d.m), uint64_t(d.lda));
+         (wide_b ? encode_bf16_2d(&maps[3], d.B, uint64_t(d.n), uint64_t(d.m), uint64_t(d.ldx))
+                 : encode_bf16_2d(&maps[3], d.B, uint64_t(d.m), uint64_t(d.m), uint64_t(d.lda)));
 }
 
 }  // namespace mo

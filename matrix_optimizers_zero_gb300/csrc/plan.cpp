@@ -64,6 +64,9 @@ int validate_muon_params(const mo_muon_params* p) {
     return MO_ERR_BAD_PARAM;
   if (p->eps < 0.f) return MO_ERR_BAD_PARAM;
   if (p->ns_steps < 1 || p->ns_steps > 100) return MO_ERR_BAD_PARAM;
+  if (p->ns_form != MO_NS_GRAM && p->ns_form != MO_NS_APPENDIX) return MO_ERR_BAD_PARAM;
+  if (p->lr_adjust != MO_LR_ORIGINAL && p->lr_adjust != MO_LR_MATCH_RMS_ADAMW) return MO_ERR_BAD_PARAM;
+  if (p->nesterov != 0 && p->nesterov != 1) return MO_ERR_BAD_PARAM;
   return MO_OK;
 }
 
@@ -143,8 +146,9 @@ void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector
   for (size_t j = 0; j < keys.size(); ++j) out[j] = keys[j].t;
 }
 
-void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L) {
+void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout& L) {
   L.n = n;
+  L.ns_form = ns_form;
   L.mats.assign(size_t(n), DevMat{});
   std::vector<int64_t> chunks(static_cast<size_t>(n), 0), casts(static_cast<size_t>(n), 0);
   int64_t nrm = 0, cast = 0;
@@ -164,6 +168,7 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L) {
     d.vec_ok = (C % 4 == 0) ? 1 : 0;
     d.cast_tiles_c = int32_t(ceil_div(C, kCastTC));
     d.shape_scale = float(std::sqrt(std::max(1.0, double(R) / double(C))));
+    d.rms_scale = float(0.2 * std::sqrt(double(std::max(R, C))));
     d.nrm_base = nrm;
     d.nrm_count = ceil_div(R * C, kNrmChunk);
     chunks[size_t(i)] = d.nrm_count;
@@ -215,6 +220,7 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L) {
     DevMat& d = L.mats[size_t(i)];
     const size_t xb = size_t(d.m) * size_t(d.ldx) * 2;
     const size_t ab = size_t(d.m) * size_t(d.lda) * 2;
+    const size_t bb = (ns_form == MO_NS_APPENDIX) ? xb : ab;
     // offsets are stored in the pointer fields until the workspace is bound
     d.X[0] = reinterpret_cast<uint16_t*>(off);
     off = align_up(off + xb, 1024);
@@ -223,7 +229,7 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L) {
     d.A = reinterpret_cast<uint16_t*>(off);
     off = align_up(off + ab, 1024);
     d.B = reinterpret_cast<uint16_t*>(off);
-    off = align_up(off + ab, 1024);
+    off = align_up(off + bb, 1024);
   }
   L.total_bytes = off;
 }

@@ -13,6 +13,7 @@ namespace mo {
 
 struct MuonLayout {
   int32_t n = 0;
+  int32_t ns_form = MO_NS_GRAM;
   std::vector<DevMat> mats;          // buffer pointers hold workspace OFFSETS until bound
   // Prologue work list: 2n segments in the order momentum/norm chunks of
   // matrix 0, of matrix 1, normalise/cast tiles of matrix 0, chunks of
@@ -43,7 +44,8 @@ int validate_adamw(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* p)
 // the output tile height (128 rows for one CTA, 256 for a CTA pair).
 void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector<TileRec>& out);
 
-// Layout of the Muon workspace for a validated table.
-void plan_muon(const mo_matrix* tbl, int32_t n, int bm, MuonLayout& L);
+// Layout of the Muon workspace for a validated table; ns_form (mo_ns_form)
+// sets the size of the B buffers (m x m, or m x n for the appendix form).
+void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout& L);
 
 }  // namespace mo

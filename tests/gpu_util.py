@@ -37,6 +37,8 @@ def shape_scale(rows, cols):
     return math.sqrt(max(1.0, rows / cols))
 
 
-def extract_update(W0, W1, lr, wd, rows, cols):
-    """Recovers the applied direction O from W1 = W0 (1 - lr wd) - lr s O."""
-    return (np.asarray(W0, np.float64) * (1.0 - lr * wd) - np.asarray(W1, np.float64)) / (lr * shape_scale(rows, cols))
+def extract_update(W0, W1, lr, wd, rows, cols, scale=None):
+    """Recovers the applied direction O from W1 = W0 (1 - lr wd) - lr s O
+    (s = sqrt(max(1, rows/cols)) unless given)."""
+    s = shape_scale(rows, cols) if scale is None else scale
+    return (np.asarray(W0, np.float64) * (1.0 - lr * wd) - np.asarray(W1, np.float64)) / (lr * s)

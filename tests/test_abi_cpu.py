@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
     assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.mo_abi_version() == 1
+    assert lib.mo_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -120,6 +120,13 @@ def test_workspace_bytes(lib):
     nb2 = lib.mo_muon_workspace_bytes(ctypes.cast(big, ctypes.c_void_p), len(g), ctypes.byref(p))
     buffers = sum(2 * min(r, c) * max(r, c) * 2 + 2 * min(r, c) ** 2 * 2 for r, c in g)
     assert buffers <= nb2 < buffers * 1.01
+    # the appendix form keeps B = A X (m x n) instead of the m x m polynomial
+    pa = mo.MuonParams(ns_form="appendix")
+    nb3 = lib.mo_muon_workspace_bytes(ctypes.cast(big, ctypes.c_void_p), len(g), ctypes.byref(pa))
+    buffers3 = sum(3 * min(r, c) * max(r, c) * 2 + min(r, c) ** 2 * 2 for r, c in g)
+    assert buffers3 <= nb3 < buffers3 * 1.01
+    assert lib.mo_muon_workspace_bytes(ctypes.cast(big, ctypes.c_void_p), len(g),
+                                       ctypes.byref(mo.MuonParams(nesterov=True, lr_adjust="match_rms_adamw"))) == nb2
 
 
 # ---------------------------------------------------------------- validation (no GPU needed)
@@ -154,7 +161,8 @@ def test_muon_validation_codes(lib):
     two[1].W = two[0].V
     assert _muon(lib, two, 2, p) == -6
     for bad in (mo.MuonParams(lr=float("nan")), mo.MuonParams(ns_steps=0), mo.MuonParams(ns_steps=101),
-                mo.MuonParams(eps=-1.0), mo.MuonParams(a=float("inf"))):
+                mo.MuonParams(eps=-1.0), mo.MuonParams(a=float("inf")), mo.MuonParams(ns_form=2),
+                mo.MuonParams(ns_form=-1), mo.MuonParams(lr_adjust=2), mo.MuonParams(nesterov=2)):
         assert _muon(lib, ok, 1, bad) == -4
     assert _muon(lib, ok, 1, p, ws=0) == -1
     assert _muon(lib, ok, 1, p, ws=(1 << 30) + 16) == -3

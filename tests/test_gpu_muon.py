@@ -29,6 +29,21 @@ def run_muon(dev_mats, params):
     assert mo.mo_last_device_error() == 0
 
 
+FORM_NAMES = {v: k for k, v in mo.NS_FORMS.items()}
+ADJUST_NAMES = {v: k for k, v in mo.LR_ADJUST.items()}
+
+
+def oracle_options(params):
+    """The oracle's keyword arguments for a MuonParams."""
+    return dict(lr=params.lr, wd=params.wd, mu=params.mu, coeffs=(params.a, params.b, params.c),
+                eps=params.eps, ns_steps=params.ns_steps, ns_form=FORM_NAMES[params.ns_form],
+                lr_adjust=ADJUST_NAMES[params.lr_adjust], nesterov=bool(params.nesterov))
+
+
+def update_scale(params, R, C):
+    return oracle.match_rms_adamw_scale(R, C) if params.lr_adjust == 1 else oracle.shape_scale(R, C)
+
+
 def check_table(host_mats, params, tol=NS_REL_FROB_TOL, direct=False):
     """Runs one step on the GPU and compares every matrix with the oracle."""
     dev = to_device(host_mats, DEV)
@@ -37,11 +52,9 @@ def check_table(host_mats, params, tol=NS_REL_FROB_TOL, direct=False):
     worst = 0.0
     for (Wh, Gh, Vh), (Wd, Gd, Vd), w0 in zip(host_mats, dev, W0):
         R, C = Wh.shape
-        Wn, Vn, O = oracle.muon_matrix_step(
-            w0, f64(Gh), f64(Vh), lr=params.lr, wd=params.wd, mu=params.mu,
-            coeffs=(params.a, params.b, params.c), eps=params.eps, ns_steps=params.ns_steps)
+        Wn, Vn, O = oracle.muon_matrix_step(w0, f64(Gh), f64(Vh), **oracle_options(params))
         assert max_rel(f64(Vd), Vn) <= FP32_MAX_REL_TOL
-        O_gpu = extract_update(w0, f64(Wd), params.lr, params.wd, R, C)
+        O_gpu = extract_update(w0, f64(Wd), params.lr, params.wd, R, C, update_scale(params, R, C))
         err = rel_frob(O_gpu, O)
         worst = max(worst, err)
         assert err <= tol, (R, C, err)
