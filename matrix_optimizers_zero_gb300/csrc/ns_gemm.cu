@@ -331,6 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The setup above overlaps the previous launch's last tiles; its outputs
+  // are read only after it has completed.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -531,13 +535,17 @@ cudaError_t launch_pair(const NsParams& p, int grid, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: CTAs start their setup (barriers, TMEM)
+  // as SMs leave the previous launch, then wait for it in griddep_wait()
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
