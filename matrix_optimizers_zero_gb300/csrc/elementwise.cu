@@ -48,6 +48,9 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
+// 16-byte vectors per thread loaded before use in each round of a norm item
+constexpr int kNrmBatch = 4;
+
 template <bool NEST>
 __device__ void prologue_norm_item(const ProParams& p, int mi, int64_t local, float* red, int* last_flag) {
   const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
@@ -59,11 +62,11 @@ __device__ void prologue_norm_item(const ProParams& p, int mi, int64_t local, fl
   const uint16_t* __restrict__ G = M.G + e0;
   float ss = 0.f;
 #pragma unroll 1
-  for (int base = 0; base < cnt; base += 8 * 256 * 4) {
-    float4 v[8];
-    uint2 g[8];
+  for (int base = 0; base < cnt; base += kNrmBatch * 256 * 4) {
+    float4 v[kNrmBatch];
+    uint2 g[kNrmBatch];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kNrmBatch; ++j) {
       const int e = base + (j * 256 + tid) * 4;
       if (e + 4 <= cnt) {
         v[j] = *reinterpret_cast<const float4*>(V + e);
@@ -71,7 +74,7 @@ __device__ void prologue_norm_item(const ProParams& p, int mi, int64_t local, fl
       }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kNrmBatch; ++j) {
       const int e = base + (j * 256 + tid) * 4;
       if (e + 4 <= cnt) {
         const float g0 = bf16_bits_to_float(g[j].x & 0xFFFFu), g1 = bf16_bits_to_float(g[j].x >> 16);
@@ -193,18 +196,35 @@ __device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, ui
   uint16_t* X = M.X[0];
   const size_t ldx = size_t(M.ldx);
   if (!M.tall) {
-    // warp w covers rows w, w+8, ...; lanes cover 4 consecutive columns each
+    // warp w covers rows w, w+8, ...; lanes cover 4 consecutive columns each.
+    // Rows go in batches of four whose loads are all issued before the
+    // batch's stores (the stores could alias the loads as far as the
+    // compiler knows, which would otherwise serialise every row on a full
+    // memory latency).
     const int c = c0 + lane * 4;
-#pragma unroll 4
-    for (int i = 0; i < kCastTR / 8; ++i) {
-      const int r = r0 + warp + 8 * i;
-      if (r >= R || c >= C) continue;
-      const size_t off = size_t(r) * size_t(C) + size_t(c);
-      uint16_t* xp = X + size_t(r) * ldx + size_t(c);
-      if (M.vec_ok && c + 4 <= C) {
-        const float4 v4 = load_u4<NEST>(p, M, off);
-        *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16x2(v4.x * sc, v4.y * sc), pack_bf16x2(v4.z * sc, v4.w * sc));
-      } else {
+    if (c < C && M.vec_ok && c + 4 <= C) {
+#pragma unroll 1
+      for (int i0 = 0; i0 < kCastTR / 8; i0 += 4) {
+        float4 u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = r0 + warp + 8 * (i0 + i);
+          if (r < R) u[i] = load_u4<NEST>(p, M, size_t(r) * size_t(C) + size_t(c));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = r0 + warp + 8 * (i0 + i);
+          if (r < R)
+            *reinterpret_cast<uint2*>(X + size_t(r) * ldx + size_t(c)) =
+                make_uint2(pack_bf16x2(u[i].x * sc, u[i].y * sc), pack_bf16x2(u[i].z * sc, u[i].w * sc));
+        }
+      }
+    } else if (c < C) {
+      for (int i = 0; i < kCastTR / 8; ++i) {
+        const int r = r0 + warp + 8 * i;
+        if (r >= R) break;
+        const size_t off = size_t(r) * size_t(C) + size_t(c);
+        uint16_t* xp = X + size_t(r) * ldx + size_t(c);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           if (c + q < C) xp[q] = float_to_bf16_bits(load_u1<NEST>(p, M, off + q) * sc);
