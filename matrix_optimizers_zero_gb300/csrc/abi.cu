@@ -208,6 +208,7 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   }
   if (E == nullptr) {
     fresh->dev = dev_id;
+    mo::order_prologue(fresh->L, int64_t(mo::kPrologueCtasPerSm) * dev->sms);
     if ((st = insert_plan(fresh, tbl, n, ws, allow_pinned)) != MO_OK) {
       delete fresh;
       return st;

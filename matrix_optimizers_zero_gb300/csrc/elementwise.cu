@@ -290,7 +290,7 @@ __device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, ui
 }
 
 template <bool NEST>
-__global__ void __launch_bounds__(256, 4) muon_prologue_kernel(const __grid_constant__ ProParams p) {
+__global__ void __launch_bounds__(256, kPrologueCtasPerSm) muon_prologue_kernel(const __grid_constant__ ProParams p) {
   ptx::griddep_launch_dependents();   // the first Gram launch may start its setup as CTAs finish
   __shared__ __align__(16) uint16_t tbuf[kCastTC][kCastTR + 8];
   __shared__ float red[8];

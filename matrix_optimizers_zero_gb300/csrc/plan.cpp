@@ -146,6 +146,34 @@ void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector
   for (size_t j = 0; j < keys.size(); ++j) out[j] = keys[j].t;
 }
 
+void order_prologue(MuonLayout& L, int64_t window) {
+  // Norm segments in table order; the cast segment of matrix i follows once
+  // `window` items (about one wave of the launch) have been listed after the
+  // last norm chunk of matrix i, so that its casts rarely wait for that norm.
+  const int32_t n = L.n;
+  L.seg_code.clear();
+  std::vector<std::pair<int32_t, int64_t>> due;   // (matrix, listed items at which its casts may start)
+  size_t head = 0;
+  int64_t listed = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    L.seg_code.push_back(2 * i);
+    listed += L.nrm_items[size_t(i)];
+    due.push_back({i, listed + window});
+    while (head < due.size() && due[head].second <= listed) {
+      L.seg_code.push_back(2 * due[head].first + 1);
+      listed += L.cast_items[size_t(due[head].first)];
+      ++head;
+    }
+  }
+  for (; head < due.size(); ++head) L.seg_code.push_back(2 * due[head].first + 1);
+  L.seg_prefix.assign(L.seg_code.size() + 1, 0);
+  for (size_t k = 0; k < L.seg_code.size(); ++k) {
+    const int32_t mat = L.seg_code[k] >> 1;
+    L.seg_prefix[k + 1] =
+        L.seg_prefix[k] + ((L.seg_code[k] & 1) ? L.cast_items[size_t(mat)] : L.nrm_items[size_t(mat)]);
+  }
+}
+
 void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout& L) {
   L.n = n;
   L.ns_form = ns_form;
@@ -178,17 +206,9 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout&
   }
   L.nrm_total = nrm;
   L.cast_total = cast;
-  L.seg_code.clear();
-  for (int32_t i = 0; i < n; ++i) {
-    L.seg_code.push_back(2 * i);
-    if (i >= 1) L.seg_code.push_back(2 * (i - 1) + 1);
-  }
-  if (n >= 1) L.seg_code.push_back(2 * (n - 1) + 1);
-  L.seg_prefix.assign(L.seg_code.size() + 1, 0);
-  for (size_t k = 0; k < L.seg_code.size(); ++k) {
-    const int32_t mat = L.seg_code[k] >> 1;
-    L.seg_prefix[k + 1] = L.seg_prefix[k] + ((L.seg_code[k] & 1) ? casts[size_t(mat)] : chunks[size_t(mat)]);
-  }
+  L.nrm_items = chunks;
+  L.cast_items = casts;
+  order_prologue(L, int64_t(kPrologueCtasPerSm) * 152);
   for (int ph = 0; ph < 3; ++ph) build_tiles(tbl, n, ph, bm, L.tiles[ph]);
 
   size_t off = 0;

@@ -15,12 +15,14 @@ struct MuonLayout {
   int32_t n = 0;
   int32_t ns_form = MO_NS_GRAM;
   std::vector<DevMat> mats;          // buffer pointers hold workspace OFFSETS until bound
-  // Prologue work list: 2n segments in the order momentum/norm chunks of
-  // matrix 0, of matrix 1, normalise/cast tiles of matrix 0, chunks of
-  // matrix 2, tiles of matrix 1, ... so that a matrix is cast right after its
-  // norm is final (while its momentum is still in L2).
+  // Prologue work list: 2n segments, the momentum/norm chunks of every
+  // matrix in table order, with the normalise/cast tiles of matrix i placed
+  // about one wave of the launch after its last chunk (order_prologue), so a
+  // matrix is cast soon after its norm is final (while its momentum is still
+  // in L2) but rarely has to wait for it.
   std::vector<int64_t> seg_prefix;   // 2n + 1 prefix sums of segment sizes
   std::vector<int32_t> seg_code;     // 2n codes: matrix * 2 + (0 = norm chunks, 1 = cast tiles)
+  std::vector<int64_t> nrm_items, cast_items;   // per matrix
   std::vector<TileRec> tiles[3];     // per phase, launch order
   int64_t nrm_total = 0;
   int64_t cast_total = 0;
@@ -43,6 +45,10 @@ int validate_adamw(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* p)
 // Tile schedule of one phase (MO_PHASE_*), sorted into launch order; bm is
 // the output tile height (128 rows for one CTA, 256 for a CTA pair).
 void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector<TileRec>& out);
+
+// (Re)orders the prologue work list for a launch that processes about
+// `window` items at a time (CTAs in flight); plan_muon uses 4 x 152.
+void order_prologue(MuonLayout& L, int64_t window);
 
 // Layout of the Muon workspace for a validated table; ns_form (mo_ns_form)
 // sets the size of the B buffers (m x m, or m x n for the appendix form).
