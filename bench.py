@@ -406,7 +406,12 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
 
-    launches_per_step = (2 + 3 * wl.ns_steps) + math.ceil(len(tail_sizes) / 256) + math.ceil(len(shapes) / 512)
+    # prologue + 3 GEMM launches per iteration; AdamW: one per 256 segments;
+    # RMNP: one per 512 entries, separately for rows shorter / not shorter
+    # than 8192 elements (warp-per-row and CTA-per-row kernels)
+    n_long = sum(1 for _, c in shapes if c >= 8192)
+    launches_per_step = ((1 + 3 * wl.ns_steps) + math.ceil(len(tail_sizes) / 256)
+                         + math.ceil((len(shapes) - n_long) / 512) + math.ceil(n_long / 512))
     peak = peaks["bf16_tflops_sustained"]
     out = {
         "metric": METRIC,

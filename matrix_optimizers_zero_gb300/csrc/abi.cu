@@ -294,33 +294,42 @@ int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmn
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MO_OK) return st;
   static thread_local mo::RmnpParams rp;   // ~25 KB: keep off the stack
-  for (int32_t b = 0; b < n; b += mo::kRmnpMaxEntries) {
-    const int32_t cnt = std::min<int32_t>(mo::kRmnpMaxEntries, n - b);
-    std::memset(&rp, 0, sizeof(rp));
-    rp.n = cnt;
-    rp.decay = float(1.0 - double(prm->lr) * double(prm->wd));
-    rp.lr = prm->lr;
-    rp.mu = prm->mu;
-    rp.eps = prm->eps;
-    int64_t rows = 0;
-    for (int32_t i = 0; i < cnt; ++i) {
-      const mo_matrix& t = tbl[b + i];
-      mo::RmnpEntry& E = rp.e[i];
-      E.W = t.W;
-      E.G = static_cast<const uint16_t*>(t.G);
-      E.V = t.V;
-      E.R = int32_t(t.rows);
-      E.C = int32_t(t.cols);
-      E.scale = scales ? scales[b + i] : float(std::sqrt(std::max(1.0, double(t.rows) / double(t.cols))));
-      E.vec_ok = (t.cols % 4 == 0) ? 1 : 0;
-      rp.row_prefix[i] = rows;
-      rows += t.rows;
+  // Two passes over the table: entries with short rows (warp per row), then
+  // entries with long rows (CTA per row); up to kRmnpMaxEntries per launch.
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool long_rows = pass == 1;
+    int32_t b = 0;
+    while (b < n) {
+      std::memset(&rp, 0, sizeof(rp));
+      rp.decay = float(1.0 - double(prm->lr) * double(prm->wd));
+      rp.lr = prm->lr;
+      rp.mu = prm->mu;
+      rp.eps = prm->eps;
+      int64_t rows = 0;
+      int32_t cnt = 0;
+      for (; b < n && cnt < mo::kRmnpMaxEntries; ++b) {
+        const mo_matrix& t = tbl[b];
+        if ((t.cols >= mo::kRmnpLongRow) != long_rows) continue;
+        mo::RmnpEntry& E = rp.e[cnt];
+        E.W = t.W;
+        E.G = static_cast<const uint16_t*>(t.G);
+        E.V = t.V;
+        E.R = int32_t(t.rows);
+        E.C = int32_t(t.cols);
+        E.scale = scales ? scales[b] : float(std::sqrt(std::max(1.0, double(t.rows) / double(t.cols))));
+        E.vec_ok = (t.cols % 4 == 0) ? 1 : 0;
+        rp.row_prefix[cnt] = rows;
+        rows += t.rows;
+        ++cnt;
+      }
+      rp.n = cnt;
+      rp.row_prefix[cnt] = rows;
+      if (cnt == 0) continue;
+      const int64_t ctas = long_rows ? rows : (rows + 7) / 8;
+      const int grid = int(std::max<int64_t>(1, std::min<int64_t>(ctas, int64_t(dev->sms) * 8)));
+      cudaError_t e = mo::launch_rmnp(rp, long_rows, grid, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
     }
-    rp.row_prefix[cnt] = rows;
-    const int64_t warps_needed = rows;
-    const int grid = int(std::max<int64_t>(1, std::min<int64_t>((warps_needed + 7) / 8, int64_t(dev->sms) * 8)));
-    cudaError_t e = mo::launch_rmnp(rp, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e);
   }
   return MO_OK;
 }

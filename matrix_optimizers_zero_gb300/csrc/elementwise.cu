@@ -407,6 +407,103 @@ __global__ void __launch_bounds__(256) rmnp_kernel(const __grid_constant__ RmnpP
   }
 }
 
+// The same RMNP step with one CTA per stored row, for long rows: a warp per
+// row keeps up to 64 rows per SM in flight, which for rows of ~14 K elements
+// (57 KB) is more than L2 holds between the two passes; a CTA per row keeps
+// 8 per SM. The row's sum of squares is reduced in a fixed order (per-thread
+// strided sums, a fixed xor tree per warp, the 8 warps in order), so a row's
+// result does not depend on the launch either.
+__global__ void __launch_bounds__(256) rmnp_row_cta_kernel(const __grid_constant__ RmnpParams p) {
+  __shared__ float red[8];
+  const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
+  const int64_t total = p.row_prefix[p.n];
+  for (int64_t row = blockIdx.x; row < total; row += gridDim.x) {
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.row_prefix[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const RmnpEntry& E = p.e[lo];
+    const int C = E.C;
+    const size_t off = size_t(row - p.row_prefix[lo]) * size_t(C);
+    float* __restrict__ Vr = E.V + off;
+    float* __restrict__ Wr = E.W + off;
+    const uint16_t* __restrict__ Gr = E.G + off;
+    float ss = 0.f;
+    if (E.vec_ok) {
+      for (int cb = tid * 4; cb < C; cb += 4 * 1024) {
+        float4 v[4];
+        uint2 g[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 1024;
+          if (cc < C) {
+            v[u] = *reinterpret_cast<const float4*>(Vr + cc);
+            g[u] = *reinterpret_cast<const uint2*>(Gr + cc);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 1024;
+          if (cc < C) {
+            float4 n4;
+            n4.x = fmaf(p.mu, v[u].x, bf16_bits_to_float(g[u].x & 0xFFFFu));
+            n4.y = fmaf(p.mu, v[u].y, bf16_bits_to_float(g[u].x >> 16));
+            n4.z = fmaf(p.mu, v[u].z, bf16_bits_to_float(g[u].y & 0xFFFFu));
+            n4.w = fmaf(p.mu, v[u].w, bf16_bits_to_float(g[u].y >> 16));
+            *reinterpret_cast<float4*>(Vr + cc) = n4;
+            ss = fmaf(n4.x, n4.x, ss);
+            ss = fmaf(n4.y, n4.y, ss);
+            ss = fmaf(n4.z, n4.z, ss);
+            ss = fmaf(n4.w, n4.w, ss);
+          }
+        }
+      }
+    } else {
+      for (int cc = tid; cc < C; cc += 256) {
+        const float vn = fmaf(p.mu, Vr[cc], bf16_bits_to_float(Gr[cc]));
+        Vr[cc] = vn;
+        ss = fmaf(vn, vn, ss);
+      }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    __syncthreads();   // red is rewritten by the next row
+    const float k = p.lr * E.scale / fmaxf(sqrtf(tot), p.eps);
+    if (E.vec_ok) {
+      for (int cb = tid * 4; cb < C; cb += 4 * 1024) {
+        float4 v[4], w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 1024;
+          if (cc < C) {
+            v[u] = *reinterpret_cast<const float4*>(Vr + cc);
+            w[u] = *reinterpret_cast<const float4*>(Wr + cc);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 1024;
+          if (cc < C) {
+            float4 o;
+            o.x = w[u].x * p.decay - k * v[u].x;
+            o.y = w[u].y * p.decay - k * v[u].y;
+            o.z = w[u].z * p.decay - k * v[u].z;
+            o.w = w[u].w * p.decay - k * v[u].w;
+            *reinterpret_cast<float4*>(Wr + cc) = o;
+          }
+        }
+      }
+    } else {
+      for (int cc = tid; cc < C; cc += 256) Wr[cc] = Wr[cc] * p.decay - k * Vr[cc];
+    }
+  }
+}
+
 // ------------------------------------------------------------------ column-cut RMNP
 //
 // Rows cut into column shards ("Optimizers In A Sharded World", section 3):
@@ -575,9 +672,12 @@ cudaError_t launch_muon_prologue(const ProParams& p, int max_grid, cudaStream_t 
   return cudaLaunchCooperativeKernel(kern, dim3(unsigned(grid)), dim3(256), args, 0, stream);
 }
 
-cudaError_t launch_rmnp(const RmnpParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_rmnp(const RmnpParams& p, bool row_per_cta, int grid, cudaStream_t stream) {
   if (p.n <= 0 || p.row_prefix[p.n] <= 0) return cudaSuccess;
-  rmnp_kernel<<<grid, 256, 0, stream>>>(p);
+  if (row_per_cta)
+    rmnp_row_cta_kernel<<<grid, 256, 0, stream>>>(p);
+  else
+    rmnp_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

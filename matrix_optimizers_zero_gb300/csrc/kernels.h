@@ -72,7 +72,10 @@ struct RmnpParams {
   int32_t n;
   float decay, lr, mu, eps;
 };
-cudaError_t launch_rmnp(const RmnpParams& p, int grid, cudaStream_t stream);
+// Rows of at least kRmnpLongRow elements go to the CTA-per-row kernel (its
+// grid: CTAs), the others to the warp-per-row kernel (grid: CTAs of 8 warps).
+constexpr int kRmnpLongRow = 8192;
+cudaError_t launch_rmnp(const RmnpParams& p, bool row_per_cta, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- column-cut RMNP
 struct ColcutParams {
