@@ -7,4 +7,4 @@ from .oracle import (NS_COEFFS, NS_EPS, RMNP_EPS, adamw_step, bf16_round, decoup
                      newton_schulz, newton_schulz_pages_form, rmnp_direction, rmnp_matrix_step,
                      rmnp_row_sharded, rmnp_table_step, shape_scale, rmnp_colcut_direction,
                      rmnp_colcut_matrix_step, RMNP_COLCUT_EPS, match_rms_adamw_scale,
-                     nesterov_direction)
+                     nesterov_direction, htrmnp_direction, htrmnp_matrix_step, HTRMNP_POWER)

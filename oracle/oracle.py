@@ -41,7 +41,9 @@ GEMM operand (X between iterations, A and B) is rounded to nearest-even bf16
 directly from float64; accumulation stays float64.
 
 Parity status: every function below is pinned by the CPU tests against
-closed forms, library routines or invariants; none is unpinned.
+closed forms, library routines or invariants, except htrmnp_direction and
+htrmnp_matrix_step: their formula is a reading of one sentence of the pages
+(parity unpinned; see their docstrings).
 """
 from __future__ import annotations
 
@@ -241,6 +243,33 @@ def rmnp_matrix_step(W, G, V, lr=0.02, wd=0.01, mu=0.95, eps=RMNP_EPS):
     R, C = np.shape(W)
     Vn = momentum(V, G, mu)
     D = rmnp_direction(Vn, eps)
+    Wn = decoupled_update(W, D, lr, wd, shape_scale(R, C))
+    return Wn, Vn, D
+
+
+HTRMNP_POWER = 0.125     # default power of the row norm ([SHARD] section 7)
+
+
+def htrmnp_direction(V: np.ndarray, power: float = HTRMNP_POWER, eps: float = RMNP_EPS) -> np.ndarray:
+    """HTRMNP direction. [SHARD] section 7 says only that HTRMNP scales RMNP's
+    row-normalised direction with a power of the row norm (p = 0.125 by
+    default); no formula is printed. Reading taken here: the row direction
+    keeps the fraction p of its norm,
+        D_i = V_i / max(||V_i||_2, eps)^(1 - p),
+    so p = 0 is RMNP and p = 1 leaves V unchanged. PARITY UNPINNED: the pages
+    fix neither the formula nor a value of it; the tests pin this reading's
+    special cases (p = 0, p = 1, degree-p homogeneity) only."""
+    V = np.asarray(V, np.float64)
+    norms = np.sqrt(np.sum(V * V, axis=1))
+    return V / (np.maximum(norms, eps) ** (1.0 - power))[:, None]
+
+
+def htrmnp_matrix_step(W, G, V, lr=0.02, wd=0.01, mu=0.95, power=HTRMNP_POWER, eps=RMNP_EPS):
+    """One HTRMNP step: momentum, the power-scaled row direction above, and
+    RMNP's shape-scaled decoupled update. Returns (W_new, V_new, D)."""
+    R, C = np.shape(W)
+    Vn = momentum(V, G, mu)
+    D = htrmnp_direction(Vn, power, eps)
     Wn = decoupled_update(W, D, lr, wd, shape_scale(R, C))
     return Wn, Vn, D
 

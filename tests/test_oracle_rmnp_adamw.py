@@ -124,3 +124,22 @@ def test_colcut_rmnp_equals_unsharded_rows():
     Z[1, 4] = 1e-9        # norm below the column-cut clamp
     D = np.concatenate(rmnp_colcut_direction([Z[:, :6], Z[:, 6:]]), axis=1)
     assert np.all(D[0] == 0) and D[1, 4] == pytest.approx(1e-9 / 1e-7, rel=1e-15)
+
+
+def test_htrmnp_reading_special_cases():
+    """HTRMNP ("Optimizers In A Sharded World", section 7) has no printed
+    formula; these pin the reading D_i = V_i / max(||V_i||, eps)^(1 - p) at
+    its special cases only (parity unpinned): p = 0 is RMNP exactly, p = 1 is
+    the identity, and the direction is homogeneous of degree p in each row."""
+    from oracle import htrmnp_direction, HTRMNP_POWER
+    assert HTRMNP_POWER == 0.125
+    rng = np.random.default_rng(31)
+    V = rng.standard_normal((23, 41)) * rng.uniform(0.01, 5, size=(23, 1))
+    assert np.array_equal(htrmnp_direction(V, power=0.0), rmnp_direction(V))
+    np.testing.assert_allclose(htrmnp_direction(V, power=1.0), V, rtol=1e-15)
+    c = rng.uniform(0.1, 10, size=(23, 1))
+    np.testing.assert_allclose(htrmnp_direction(c * V), c ** 0.125 * htrmnp_direction(V), rtol=1e-13)
+    norms = np.linalg.norm(htrmnp_direction(V), axis=1)
+    np.testing.assert_allclose(norms, np.linalg.norm(V, axis=1) ** 0.125, rtol=1e-13)
+    Z = np.zeros((2, 5))
+    assert np.all(htrmnp_direction(Z) == 0)
