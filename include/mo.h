@@ -187,6 +187,17 @@ int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cud
 int rmnp_step_scaled(const mo_matrix* tbl, const float* scales, int32_t n,
                      const mo_rmnp_params* params, cudaStream_t stream);
 
+/* HTRMNP: RMNP whose row direction keeps a power of the row norm.
+ * "Optimizers In A Sharded World" section 7 says HTRMNP scales the row
+ * direction with a power of the row norm, p = 0.125 by default, and prints no
+ * formula; this library takes the reading
+ *   V <- mu V + G;  D_i = V_i / max(||V_i||_2, eps)^(1 - power);
+ *   W <- W (1 - lr wd) - lr sqrt(max(1, rows/cols)) D,
+ * so power = 0 is rmnp_step and power = 1 applies the momentum itself.
+ * Arguments and layout as rmnp_step; power must be in [0, 1]
+ * (MO_ERR_BAD_PARAM otherwise). */
+int htrmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, float power, cudaStream_t stream);
+
 /* RMNP with rows cut into column shards ("Optimizers In A Sharded World",
  * section 3, column-cut tensor parallelism, and the appendix's column-cut
  * scheme), evaluated on one GPU: each table entry is one dense column shard

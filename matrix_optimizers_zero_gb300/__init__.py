@@ -18,7 +18,7 @@ from .build import LIB_PATH
 __all__ = [
     "MoError", "MuonParams", "RmnpParams", "AdamWParams", "load_library",
     "mo_muon_workspace_bytes", "muon_workspace", "muon_owner_step", "muon_owner_step_timed",
-    "rmnp_step", "rmnp_step_scaled", "adamw_tail_step", "mo_last_device_error",
+    "rmnp_step", "rmnp_step_scaled", "htrmnp_step", "adamw_tail_step", "mo_last_device_error",
     "mo_status_string", "mo_selftest_bounded_wait", "mo_muon_tile_schedule", "MuonTable",
     "TailTable", "RmnpTable", "muon_owner_step_noalloc", "mo_static_scratch_bytes", "mo_plan_owners",
     "rmnp_colcut_step",
@@ -113,6 +113,7 @@ def load_library() -> ctypes.CDLL:
         "adamw_tail_step": (ctypes.c_int, [P, I32, P, P]),
         "rmnp_step": (ctypes.c_int, [P, I32, P, P]),
         "rmnp_step_scaled": (ctypes.c_int, [P, P, I32, P, P]),
+        "htrmnp_step": (ctypes.c_int, [P, I32, P, ctypes.c_float, P]),
         "mo_last_device_error": (ctypes.c_int, [P]),
         "mo_last_cuda_error": (ctypes.c_int, []),
         "mo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -261,6 +262,17 @@ def rmnp_step(mats, params: Optional[RmnpParams] = None, stream=None) -> None:
     t = _as_table(mats)
     params = params or RmnpParams()
     _check(load_library().rmnp_step(t.ptr, t.n, ctypes.byref(params), _stream_ptr(stream)), "rmnp_step")
+
+
+HTRMNP_POWER = 0.125
+
+
+def htrmnp_step(mats, params: Optional[RmnpParams] = None, power: float = HTRMNP_POWER, stream=None) -> None:
+    """RMNP with the row direction scaled by ||V_i||^power (see include/mo.h)."""
+    t = _as_table(mats)
+    params = params or RmnpParams()
+    _check(load_library().htrmnp_step(t.ptr, t.n, ctypes.byref(params), float(power), _stream_ptr(stream)),
+           "htrmnp_step")
 
 
 def rmnp_step_scaled(mats, scales: Sequence[float], params: Optional[RmnpParams] = None, stream=None) -> None:

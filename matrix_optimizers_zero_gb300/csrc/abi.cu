@@ -282,10 +282,11 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
 
 namespace {
 
-int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmnp_params* prm,
+int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmnp_params* prm, float power,
               cudaStream_t stream) {
   int st = mo::validate_rmnp_params(prm);
   if (st != MO_OK) return st;
+  if (!std::isfinite(power) || power < 0.f || power > 1.f) return MO_ERR_BAD_PARAM;
   if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
   if (scales)
     for (int32_t i = 0; i < n; ++i)
@@ -305,6 +306,7 @@ int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmn
       rp.lr = prm->lr;
       rp.mu = prm->mu;
       rp.eps = prm->eps;
+      rp.power = power;
       int64_t rows = 0;
       int32_t cnt = 0;
       for (; b < n && cnt < mo::kRmnpMaxEntries; ++b) {
@@ -362,13 +364,17 @@ int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params*
 }
 
 int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cudaStream_t stream) {
-  return rmnp_impl(tbl, nullptr, n, params, stream);
+  return rmnp_impl(tbl, nullptr, n, params, 0.0f, stream);
 }
 
 int rmnp_step_scaled(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmnp_params* params,
                      cudaStream_t stream) {
   if (n > 0 && !scales) return MO_ERR_NULL_POINTER;
-  return rmnp_impl(tbl, scales, n, params, stream);
+  return rmnp_impl(tbl, scales, n, params, 0.0f, stream);
+}
+
+int htrmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, float power, cudaStream_t stream) {
+  return rmnp_impl(tbl, nullptr, n, params, power, stream);
 }
 
 size_t mo_rmnp_colcut_workspace_bytes(const mo_matrix* shards, int32_t n) {

@@ -314,6 +314,14 @@ __global__ void __launch_bounds__(256, kPrologueCtasPerSm) muon_prologue_kernel(
 }
 
 // ------------------------------------------------------------------ RMNP
+
+// lr s / max(||V_i||, eps) for RMNP; lr s max(||V_i||, eps)^(power - 1) for
+// HTRMNP (a reading of "Optimizers In A Sharded World" section 7, which names
+// the power scaling without printing a formula).
+__device__ __forceinline__ float rmnp_factor(const RmnpParams& p, float scale, float sum_sq) {
+  const float nrm = fmaxf(sqrtf(sum_sq), p.eps);
+  return p.power == 0.0f ? p.lr * scale / nrm : p.lr * scale * powf(nrm, p.power - 1.0f);
+}
 //
 // One warp per stored row ("Optimizers In A Sharded World", section 1 and the
 // appendix rmnp_local): V_i <- mu V_i + G_i, D_i = V_i / max(||V_i||_2, eps),
@@ -376,7 +384,7 @@ __global__ void __launch_bounds__(256) rmnp_kernel(const __grid_constant__ RmnpP
       }
     }
     ss = warp_sum(ss);
-    const float k = p.lr * E.scale / fmaxf(sqrtf(ss), p.eps);
+    const float k = rmnp_factor(p, E.scale, ss);
     if (E.vec_ok) {
       for (int cb = lane * 4; cb < C; cb += 4 * 128) {
         float4 v[4], w[4];
@@ -473,7 +481,7 @@ __global__ void __launch_bounds__(256) rmnp_row_cta_kernel(const __grid_constant
 #pragma unroll
     for (int w = 0; w < 8; ++w) tot += red[w];
     __syncthreads();   // red is rewritten by the next row
-    const float k = p.lr * E.scale / fmaxf(sqrtf(tot), p.eps);
+    const float k = rmnp_factor(p, E.scale, tot);
     if (E.vec_ok) {
       for (int cb = tid * 4; cb < C; cb += 4 * 1024) {
         float4 v[4], w[4];

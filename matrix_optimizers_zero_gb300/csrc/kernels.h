@@ -71,6 +71,7 @@ struct RmnpParams {
   int64_t row_prefix[kRmnpMaxEntries + 1];
   int32_t n;
   float decay, lr, mu, eps;
+  float power;                // HTRMNP: rows scaled by max(||V_i||, eps)^(power - 1); 0 for RMNP
 };
 // Rows of at least kRmnpLongRow elements go to the CTA-per-row kernel (its
 // grid: CTAs), the others to the warp-per-row kernel (grid: CTAs of 8 warps).

@@ -195,3 +195,7 @@ def test_adamw_and_rmnp_validation_codes(lib):
     assert lib.rmnp_step_scaled(tp, None, 1, ctypes.byref(mo.RmnpParams()), None) == -1
     sc = (ctypes.c_float * 1)(float("nan"))
     assert lib.rmnp_step_scaled(tp, ctypes.cast(sc, ctypes.c_void_p), 1, ctypes.byref(mo.RmnpParams()), None) == -4
+    for bad_power in (-0.1, 1.5, float("nan"), float("inf")):
+        assert lib.htrmnp_step(tp, 1, ctypes.byref(mo.RmnpParams()), ctypes.c_float(bad_power), None) == -4
+    assert lib.htrmnp_step(None, 0, ctypes.byref(mo.RmnpParams()), ctypes.c_float(0.125), None) == 0
+    assert lib.htrmnp_step(tp, 1, ctypes.byref(mo.RmnpParams(eps=-1.0)), ctypes.c_float(0.125), None) == -4

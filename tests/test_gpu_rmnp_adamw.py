@@ -206,3 +206,46 @@ def test_rmnp_colcut_validation():
         mo.rmnp_colcut_step([(W, G, V), (W2, G2, V2), (W.clone(), G.clone(), V.clone())], [0, 1, 0], [1, 1, 1])
     with pytest.raises(mo.MoError):      # shards of one matrix with different rows
         mo.rmnp_colcut_step([(W, G, V), (W2[:4], G2[:4], V2[:4])], [0, 0], [1, 1])
+
+
+# ---------------------------------------------------------------- HTRMNP (a reading: see include/mo.h)
+
+@pytest.mark.parametrize("shape", [(130, 257), (1, 9), (33, 4096), (16, 27648), (5, 14336), (7, 130)])
+@pytest.mark.parametrize("power", [0.125, 0.5])
+def test_htrmnp_direction(shape, power):
+    """W = 0, lr = 1, wd = 0 exposes -s D; rows of 8192 elements or more run
+    on the CTA-per-row kernel, the others on the warp-per-row one."""
+    wl = workloads.custom_workload([shape], w_std=0.0, g_std=1.0)
+    host = [workloads.host_matrix(wl, 0, v_std=0.5)]
+    dev = to_device(host, DEV)
+    mo.htrmnp_step(dev, mo.RmnpParams(lr=1.0, wd=0.0, mu=0.9), power=power)
+    torch.cuda.synchronize()
+    W, G, V = host[0]
+    _, Vn, D = oracle.htrmnp_matrix_step(f64(W), f64(G), f64(V), lr=1.0, wd=0.0, mu=0.9, power=power)
+    got = -f64(dev[0][0]) / shape_scale(*shape)
+    assert max_rel(got, D) <= FP32_MAX_REL_TOL
+    assert max_rel(f64(dev[0][2]), Vn) <= FP32_MAX_REL_TOL
+
+
+def test_htrmnp_power_zero_is_rmnp_bit_exactly():
+    wl = workloads.custom_workload([(64, 1280), (17, 9000)], g_std=1e-3)
+    host = [workloads.host_matrix(wl, i, v_std=1e-3) for i in range(2)]
+    a, b = to_device(host, DEV), to_device(host, DEV)
+    mo.rmnp_step(a, mo.RmnpParams())
+    mo.htrmnp_step(b, mo.RmnpParams(), power=0.0)
+    torch.cuda.synchronize()
+    for (Wa, _, Va), (Wb, _, Vb) in zip(a, b):
+        assert torch.equal(Wa, Wb) and torch.equal(Va, Vb)
+
+
+def test_htrmnp_gpt2l_layer():
+    wl = workloads.get_workload("gpt2l")
+    host = [workloads.host_matrix(wl, i, v_std=1e-3) for i in range(4)]
+    dev = to_device(host, DEV)
+    p = mo.RmnpParams()
+    mo.htrmnp_step(dev, p)
+    torch.cuda.synchronize()
+    for (Wh, Gh, Vh), (Wd, _, Vd) in zip(host, dev):
+        Wn, Vn, _ = oracle.htrmnp_matrix_step(f64(Wh), f64(Gh), f64(Vh), lr=p.lr, wd=p.wd, mu=p.mu, eps=p.eps)
+        assert max_rel(f64(Vd), Vn) <= FP32_MAX_REL_TOL
+        assert max_rel(f64(Wd), Wn) <= FP32_MAX_REL_TOL
