@@ -6,6 +6,21 @@ marshals torch tensors into the C tables and raises on error statuses. Every
 step of the computation runs in the library's CUDA kernels; there is no
 Python or CPU fallback, and importing the binding fails loudly when the
 library has not been built (python -m matrix_optimizers_zero_gb300.build).
+
+Typical use on one owner (tensors on the current CUDA device; W and V fp32,
+G bf16, all of shape [rows, cols], contiguous):
+
+    import matrix_optimizers_zero_gb300 as mo
+    mats = [(W, G, V) for ...]                    # the owner's 2D matrices
+    p = mo.MuonParams(lr=0.02, wd=0.01, mu=0.95)  # ns_form / lr_adjust / nesterov for the variants
+    ws = mo.muon_workspace(mats, p)               # reuse it across steps
+    mo.muon_owner_step(mats, p, ws)               # momentum, Newton-Schulz, weight update
+    mo.adamw_tail_step(segments, mo.AdamWParams(step=t))
+    mo.rmnp_step(mats_rmnp, mo.RmnpParams())
+    assert mo.mo_last_device_error() == 0         # synchronises; bounded device waits
+
+Plans (tile schedules, tensor maps) are cached per (table, workspace), so a
+training loop that passes the same tensors every step plans once.
 """
 from __future__ import annotations
 
