@@ -36,7 +36,7 @@ METRIC = "owner Muon step ms & NS TFLOP/s vs bf16 peak; RMNP/AdamW HBM GB/s"
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the four-layer
 # table scaled x9 by matrices (profiles/ns_gemm_pair_gpt2l_4layers_full.md).
 # Valid only for the kernel source it was measured on.
-NS_TRAFFIC = {"source_sha256_16": "32577f0e7e91447a", "workload": "gpt2l", "bytes_per_ns_segment": 29.97e9}
+NS_TRAFFIC = {"source_sha256_16": "2d78d41360a4adcd", "workload": "gpt2l", "bytes_per_ns_segment": 36.02e9}
 UNIT = "TFLOP/s"
 
 
@@ -53,11 +53,14 @@ def load_peaks():
 
 def ns_traffic(workload: str):
     """The profiled DRAM traffic of the NS launches, or None when the kernel
-    source differs from the one profiled (or for another workload)."""
+    or its tile schedule differs from the one profiled (or for another
+    workload)."""
     import hashlib
-    path = os.path.join(ROOT, "matrix_optimizers_zero_gb300", "csrc", "ns_gemm.cu")
-    digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
-    if digest != NS_TRAFFIC["source_sha256_16"] or workload != NS_TRAFFIC["workload"]:
+    h = hashlib.sha256()
+    for name in ("ns_gemm.cu", "plan.cpp"):
+        with open(os.path.join(ROOT, "matrix_optimizers_zero_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != NS_TRAFFIC["source_sha256_16"] or workload != NS_TRAFFIC["workload"]:
         return None
     return NS_TRAFFIC["bytes_per_ns_segment"]
 
@@ -456,7 +459,7 @@ def run_ours(args, rank, world, local_rank):
             "unit": "TFLOP/s",
             "frac": round(ns_tflops / peak, 4),
             "traffic": ns_traffic(wl.name),
-            "traffic_unit": "DRAM bytes per step's NS launches (ncu, 4-layer capture x9)",
+            "traffic_unit": "DRAM bytes per step's 15 NS launches (ncu, full table, single-pass metrics)",
             "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
         },
         "e2e": ({"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),

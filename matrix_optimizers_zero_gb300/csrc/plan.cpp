@@ -136,9 +136,20 @@ void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector
           if ((tn + 1) * kBN > tm * bm) keys.push_back({k, {uint32_t(i), uint16_t(tm), uint16_t(tn)}});
     }
   }
-  std::sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
+  // Longest K first, then by matrix. Within a matrix the symmetric phases go
+  // row-block by row-block; the m x n products go column-block by
+  // column-block, so the tiles in flight at once share a few X column panels
+  // and all of B's rows (on the 8B table's 4096 x 14336 matrices the
+  // row-major order kept ~70 panels of 2 MB in flight, more than L2 holds;
+  // measured 5.7% faster NS there, neutral on GPT-2 Large).
+  const bool col_major = phase == MO_PHASE_UPDATE;
+  std::sort(keys.begin(), keys.end(), [col_major](const Key& a, const Key& b) {
     if (a.k != b.k) return a.k > b.k;
     if (a.t.mat != b.t.mat) return a.t.mat < b.t.mat;
+    if (col_major) {
+      if (a.t.tn != b.t.tn) return a.t.tn < b.t.tn;
+      return a.t.tm < b.t.tm;
+    }
     if (a.t.tm != b.t.tm) return a.t.tm < b.t.tm;
     return a.t.tn < b.t.tn;
   });

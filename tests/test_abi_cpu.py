@@ -57,9 +57,10 @@ def py_schedule(shapes, phase):
         m, n = min(R, C), max(R, C)
         tiles_m = -(-m // BM)
         if phase == mo.PHASE_UPDATE:
+            # m x n products: column-block by column-block within a matrix
             for tm in range(tiles_m):
                 for tn in range(-(-n // 256)):
-                    keys.append((-m, i, tm, tn))
+                    keys.append((-m, i, tn, tm))
         else:
             k = n if phase == mo.PHASE_GRAM else m
             for tm in range(tiles_m):
@@ -67,6 +68,8 @@ def py_schedule(shapes, phase):
                     if (tn + 1) * 256 > tm * BM:
                         keys.append((-k, i, tm, tn))
     keys.sort()
+    if phase == mo.PHASE_UPDATE:
+        return [(i, tm, tn) for _, i, tn, tm in keys]
     return [(i, tm, tn) for _, i, tm, tn in keys]
 
 
