@@ -244,8 +244,9 @@ enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
  * and the tile count into *count. Returns MO_OK, or MO_ERR_BAD_SHAPE if cap is
  * too small (then *count holds the required size). Tiles are sorted by
  * decreasing reduction length K (n for the Gram, m otherwise), ties broken by
- * table index, then tile row, then tile column. Gram and A.A tiles cover only
- * tiles that touch the upper triangle (col_end > row_begin). */
+ * table index, then tile row and tile column (Gram, A.A) or tile column and
+ * tile row (B.X). Gram and A.A tiles cover only tiles that touch the upper
+ * triangle (col_end > row_begin). */
 int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase,
                           mo_tile* out, int64_t cap, int64_t* count);
 
