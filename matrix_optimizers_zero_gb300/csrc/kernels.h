@@ -29,7 +29,6 @@ struct NsParams {
 // phase: MO_PHASE_GRAM, MO_PHASE_POLY, MO_PHASE_UPDATE, kPhaseAX or kPhaseABX;
 // last (UPDATE and ABX only) applies the weight update in the epilogue.
 cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream);
-size_t ns_gemm_smem_bytes();
 // Writes kMapsPerMat CUtensorMap; with MO_NS_APPENDIX the B buffer is m x n.
 bool encode_matrix_maps(const DevMat& d, int ns_form, void* out_maps);
 cudaError_t device_status_ptr(int** out);

@@ -557,8 +557,6 @@ cudaError_t launch_pair(const NsParams& p, int grid, cudaStream_t stream) {
 
 }  // namespace
 
-size_t ns_gemm_smem_bytes() { return kPairSmem; }
-
 cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream) {
   if (p.ntiles <= 0) return cudaSuccess;
   switch (phase) {
