@@ -42,3 +42,27 @@ def extract_update(W0, W1, lr, wd, rows, cols, scale=None):
     (s = sqrt(max(1, rows/cols)) unless given)."""
     s = shape_scale(rows, cols) if scale is None else scale
     return (np.asarray(W0, np.float64) * (1.0 - lr * wd) - np.asarray(W1, np.float64)) / (lr * s)
+
+
+def fp32_accumulation_noise(X0, O_ref, coeffs, steps):
+    """Relative Frobenius distance between the oracle's rounded iteration O_ref
+    and the same iteration (bf16 at the same points) with fp32 instead of fp64
+    accumulation, computed with NumPy float32 products. It measures how far
+    the bf16 rounding decisions alone move a correct fp32-accumulating
+    implementation from the oracle on this input (a rounding boundary that
+    fp32 and fp64 sums fall on different sides of flips one bf16 value, and
+    the iteration amplifies small singular directions)."""
+    import oracle
+    a, b, c = (np.float32(t) for t in coeffs)
+    X = np.asarray(X0, np.float64)
+    tall = X.shape[0] > X.shape[1]
+    if tall:
+        X = X.T
+    X = oracle.bf16_round(X).astype(np.float32)
+    for k in range(steps):
+        A = oracle.bf16_round((X @ X.T).astype(np.float64)).astype(np.float32)
+        B = oracle.bf16_round((b * A + c * (A @ A)).astype(np.float64)).astype(np.float32)
+        Xn = a * X + B @ X
+        X = oracle.bf16_round(Xn.astype(np.float64)).astype(np.float32) if k < steps - 1 else Xn
+    X = X.astype(np.float64)
+    return rel_frob(X.T if tall else X, O_ref)

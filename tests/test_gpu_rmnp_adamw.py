@@ -249,3 +249,13 @@ def test_htrmnp_gpt2l_layer():
         Wn, Vn, _ = oracle.htrmnp_matrix_step(f64(Wh), f64(Gh), f64(Vh), lr=p.lr, wd=p.wd, mu=p.mu, eps=p.eps)
         assert max_rel(f64(Vd), Vn) <= FP32_MAX_REL_TOL
         assert max_rel(f64(Wd), Wn) <= FP32_MAX_REL_TOL
+
+
+def test_rmnp_more_than_one_launch_of_entries():
+    """700 entries (two launches of at most 512), short and long rows mixed
+    (both RMNP kernels, each with its own launches)."""
+    rng = np.random.default_rng(78)
+    shapes = [(int(rng.integers(1, 9)), int(rng.choice([7, 64, 1000, 8192, 9001]))) for _ in range(700)]
+    wl = workloads.custom_workload(shapes, g_std=1e-3)
+    host = [workloads.host_matrix(wl, i, v_std=1e-3) for i in range(len(shapes))]
+    rmnp_check(host, mo.RmnpParams())
