@@ -316,6 +316,9 @@ def run_ours(args, rank, world, local_rank):
     muon_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
     adam_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
     rmnp_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in evs)
+    # per-step minima (each step's events from its Muon start to its RMNP end)
+    step_min_ms = min(e[0].elapsed_time(e[5]) for e in evs)
+    ns_min_ms = min(e[1].elapsed_time(e[2]) for e in evs)
 
     ns_flops = workloads.workload_alg_flops(wl)
     ns_dense = sum(workloads.ns_dense_flops(r, c, wl.ns_steps) for r, c in shapes)
@@ -450,6 +453,10 @@ def run_ours(args, rank, world, local_rank):
             "rmnp_ms": round(rmnp_ms, 4),
             "rmnp_gbs": round(rmnp_gbs, 1),
             "rmnp_frac_hbm": round(rmnp_gbs / peaks["hbm_gbs"], 4),
+            "means_over_steps": args.steps,
+            "step_min_ms": round(step_min_ms, 4),
+            "ns_min_ms": round(ns_min_ms, 4),
+            "ns_tflops_alg_best": round(ns_flops / (ns_min_ms * 1e-3) / 1e12, 2),
         },
         "roofline": {
             "bound": "tensor",
