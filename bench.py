@@ -36,7 +36,7 @@ METRIC = "owner Muon step ms & NS TFLOP/s vs bf16 peak; RMNP/AdamW HBM GB/s"
 # from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the four-layer
 # table scaled x9 by matrices (profiles/ns_gemm_pair_gpt2l_4layers_full.md).
 # Valid only for the kernel source it was measured on.
-NS_TRAFFIC = {"source_sha256_16": "2d78d41360a4adcd", "workload": "gpt2l", "bytes_per_ns_segment": 36.02e9}
+NS_TRAFFIC = {"source_sha256_16": "adc0df84ce3d0526", "workload": "gpt2l", "bytes_per_ns_segment": 36.27e9}
 UNIT = "TFLOP/s"
 
 
