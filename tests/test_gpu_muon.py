@@ -271,3 +271,44 @@ def test_ten_iterations():
         err = rel_frob(extract_update(w0, f64(Wd), p.lr, p.wd, R, C), O)
         noise = fp32_accumulation_noise(oracle.frobenius_normalize(Vn, p.eps), O, (p.a, p.b, p.c), p.ns_steps)
         assert err <= max(NS_REL_FROB_TOL, 1.5 * noise), (R, C, err, noise)
+
+
+def test_two_host_threads_two_streams():
+    """Two host threads each run Muon steps on their own table, workspace and
+    stream at the same time (the plan cache is shared and locked); both match
+    the oracle."""
+    import threading
+    tables = []
+    for seed_shapes in ([(256, 640), (640, 256)], [(384, 384), (130, 700)]):
+        wl = workloads.custom_workload(seed_shapes, g_std=1e-3)
+        host = [workloads.host_matrix(wl, i, v_std=1e-3) for i in range(len(seed_shapes))]
+        tables.append(host)
+    p = mo.MuonParams()
+    devs = [to_device(h, DEV) for h in tables]
+    W0 = [[f64(W) for W, _, _ in h] for h in tables]
+    errors = []
+
+    def work(k):
+        try:
+            torch.cuda.set_device(DEV)
+            s = torch.cuda.Stream(DEV)
+            ws = mo.muon_workspace(devs[k], p, device=DEV)
+            with torch.cuda.stream(s):
+                mo.muon_owner_step(devs[k], p, ws, stream=s)
+            s.synchronize()
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert mo.mo_last_device_error() == 0
+    for host, dev, w0s in zip(tables, devs, W0):
+        for (Wh, Gh, Vh), (Wd, _, Vd), w0 in zip(host, dev, w0s):
+            R, C = Wh.shape
+            _, Vn, O = oracle.muon_matrix_step(w0, f64(Gh), f64(Vh), **oracle_options(p))
+            assert max_rel(f64(Vd), Vn) <= FP32_MAX_REL_TOL
+            assert rel_frob(extract_update(w0, f64(Wd), p.lr, p.wd, R, C), O) <= NS_REL_FROB_TOL
