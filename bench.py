@@ -409,6 +409,9 @@ def run_ours(args, rank, world, local_rank):
     if mo.mo_last_device_error() != 0:
         raise RuntimeError("device-side timeout during the timed region")
 
+    extras = measure_extras(args, mo, workloads, wl, shapes, W_l, G_l, V_l, Wr_l, Vr_l, dev, stream, peaks) \
+        if args.extras else None
+
     if rank != 0:
         return None
 
@@ -475,12 +478,113 @@ def run_ours(args, rank, world, local_rank):
                            "gradients double-buffered on the device"}
                 if e2e_steps else None),
         "gpu_launches": int(launches_per_step * args.steps),
+        **({"extras": extras} if extras is not None else {}),
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
         v, secs, desc, cores = cpu_oracle_sample(wl, max_seconds=args.cpu_seconds, min_seconds=10.0)
         out["cpu_baseline"] = {"value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": desc, "seconds": round(secs, 2)}
+    return out
+
+
+# ---------------------------------------------------------------- next-row kernels (--extras)
+
+def measure_extras(args, mo, workloads, wl, shapes, W_l, G_l, V_l, Wr_l, Vr_l, dev, stream, peaks):
+    """Times the kernels beyond the benchmarked step on the same table (not
+    part of the headline step): the Muon variants, column-cut RMNP, HTRMNP and
+    the host-side owner planner. CUDA events on `stream`, 2 warm-up + 5 timed
+    calls each."""
+    import time
+    import torch
+
+    def timed(fn, reps=5, warm=2):
+        for _ in range(warm):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    out = {}
+    mats = list(zip(W_l, G_l, V_l))
+    table = mo.MuonTable(mats)
+    n_el = sum(r * c for r, c in shapes)
+
+    def muon_variant(name, params, flops):
+        ws = mo.muon_workspace(table, params, device=dev)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for e in evs:
+            e.record(stream)
+        ns = []
+
+        def call():
+            mo.muon_owner_step_timed(table, params, ws, evs[0], evs[1], stream=stream)
+
+        total = timed(call)
+        for _ in range(3):
+            call()
+            torch.cuda.synchronize(dev)
+            ns.append(evs[0].elapsed_time(evs[1]))
+        ns_ms = min(ns)
+        out[name] = {"muon_step_ms": round(total, 4), "ns_ms": round(ns_ms, 4),
+                     "ns_tflops_alg": round(flops / (ns_ms * 1e-3) / 1e12, 2),
+                     "ns_frac_of_sustained_peak": round(flops / (ns_ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"], 4)}
+
+    mn = [(min(r, c), max(r, c)) for r, c in shapes]
+    muon_variant("muon_appendix_form", mo.MuonParams(lr=wl.lr, wd=wl.wd, mu=wl.mu, ns_form="appendix"),
+                 sum(5 * 5 * m * m * n for m, n in mn))
+    out["muon_appendix_form"]["flops_note"] = "5 iterations x (m^2 n Gram + 2 m^2 n A.X + 2 m^2 n A.B)"
+    muon_variant("muon_convergence_settings",
+                 mo.MuonParams(lr=1e-3, wd=1e-2, mu=0.5, ns_steps=2, lr_adjust="match_rms_adamw", nesterov=True),
+                 sum(2 * (3 * m * m * n + m ** 3) for m, n in mn))
+
+    # HTRMNP on the RMNP copy of the table, 18 bytes per element like RMNP
+    rtable = mo.MuonTable(list(zip(Wr_l, G_l, Vr_l)))
+    ms = timed(lambda: mo.htrmnp_step(rtable, mo.RmnpParams(lr=wl.lr, wd=wl.wd, mu=wl.mu), stream=stream))
+    gbs = n_el * workloads.RMNP_BYTES_PER_EL / (ms * 1e-3) / 1e9
+    out["htrmnp"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+
+    # column-cut RMNP: every matrix cut into 4 column shards (own buffers)
+    shards, groups, scales = [], [], []
+    for g_id, (r, c) in enumerate(shapes):
+        edges = [c * k // 4 for k in range(5)]
+        for a, b in zip(edges[:-1], edges[1:]):
+            if b > a:
+                shards.append((torch.empty(r, b - a, device=dev).normal_(0, wl.w_std),
+                               torch.empty(r, b - a, device=dev).normal_(0, wl.g_std).to(torch.bfloat16),
+                               torch.zeros(r, b - a, device=dev)))
+                groups.append(g_id)
+                scales.append(max(1.0, r / c) ** 0.5)
+    chunks = []
+    k = 0
+    while k < len(shards):                       # at most 512 shards per call, whole groups
+        j = min(len(shards), k + 512)
+        while j < len(shards) and j > k and groups[j] == groups[j - 1]:
+            j -= 1
+        chunks.append((k, j))
+        k = j
+    cp = mo.RmnpParams(lr=wl.lr, wd=wl.wd, mu=wl.mu, eps=1e-7)
+
+    def colcut():
+        for a, b in chunks:
+            mo.rmnp_colcut_step(shards[a:b], groups[a:b], scales[a:b], cp, stream=stream)
+
+    ms = timed(colcut)
+    gbs = n_el * 22 / (ms * 1e-3) / 1e9
+    out["rmnp_colcut_4_shards"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                                   "bytes_per_el": 22}
+
+    # owner planner (host only): GPT-2 Large-style roles over 8 ranks
+    roles = workloads.owner_roles(wl, 4 if len(shapes) % 4 == 0 else 1)
+    t0 = time.perf_counter()
+    for _ in range(20):
+        mo.mo_plan_owners(roles, 8)
+    out["owner_planner_8_ranks_us"] = round((time.perf_counter() - t0) / 20 * 1e6, 1)
     return out
 
 
@@ -531,6 +635,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=25.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop (profiling runs)")
+    ap.add_argument("--extras", action="store_true",
+                    help="also time the next-row kernels (Muon variants, column-cut RMNP, HTRMNP, planner)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
