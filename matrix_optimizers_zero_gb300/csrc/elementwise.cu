@@ -544,19 +544,34 @@ __global__ void __launch_bounds__(256) colcut_partial_kernel(const __grid_consta
     const uint16_t* __restrict__ Gr = E.G + off;
     float ss = 0.f;
     if (E.vec_ok) {
-      for (int cc = lane * 4; cc < C; cc += 128) {
-        const float4 v = *reinterpret_cast<const float4*>(Vr + cc);
-        const uint2 g = *reinterpret_cast<const uint2*>(Gr + cc);
-        float4 n4;
-        n4.x = fmaf(p.mu, v.x, bf16_bits_to_float(g.x & 0xFFFFu));
-        n4.y = fmaf(p.mu, v.y, bf16_bits_to_float(g.x >> 16));
-        n4.z = fmaf(p.mu, v.z, bf16_bits_to_float(g.y & 0xFFFFu));
-        n4.w = fmaf(p.mu, v.w, bf16_bits_to_float(g.y >> 16));
-        *reinterpret_cast<float4*>(Vr + cc) = n4;
-        ss = fmaf(n4.x, n4.x, ss);
-        ss = fmaf(n4.y, n4.y, ss);
-        ss = fmaf(n4.z, n4.z, ss);
-        ss = fmaf(n4.w, n4.w, ss);
+      // four 16-byte vectors per lane, all loaded before use
+      for (int cb = lane * 4; cb < C; cb += 4 * 128) {
+        float4 v[4];
+        uint2 g[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 128;
+          if (cc < C) {
+            v[u] = *reinterpret_cast<const float4*>(Vr + cc);
+            g[u] = *reinterpret_cast<const uint2*>(Gr + cc);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 128;
+          if (cc < C) {
+            float4 n4;
+            n4.x = fmaf(p.mu, v[u].x, bf16_bits_to_float(g[u].x & 0xFFFFu));
+            n4.y = fmaf(p.mu, v[u].y, bf16_bits_to_float(g[u].x >> 16));
+            n4.z = fmaf(p.mu, v[u].z, bf16_bits_to_float(g[u].y & 0xFFFFu));
+            n4.w = fmaf(p.mu, v[u].w, bf16_bits_to_float(g[u].y >> 16));
+            *reinterpret_cast<float4*>(Vr + cc) = n4;
+            ss = fmaf(n4.x, n4.x, ss);
+            ss = fmaf(n4.y, n4.y, ss);
+            ss = fmaf(n4.z, n4.z, ss);
+            ss = fmaf(n4.w, n4.w, ss);
+          }
+        }
       }
     } else {
       for (int cc = lane; cc < C; cc += 32) {
@@ -587,14 +602,28 @@ __global__ void __launch_bounds__(256) colcut_apply_kernel(const __grid_constant
     const float* __restrict__ Vr = E.V + off;
     float* __restrict__ Wr = E.W + off;
     if (E.vec_ok) {
-      for (int cc = lane * 4; cc < C; cc += 128) {
-        const float4 v = *reinterpret_cast<const float4*>(Vr + cc);
-        float4 w = *reinterpret_cast<const float4*>(Wr + cc);
-        w.x = w.x * p.decay - k * v.x;
-        w.y = w.y * p.decay - k * v.y;
-        w.z = w.z * p.decay - k * v.z;
-        w.w = w.w * p.decay - k * v.w;
-        *reinterpret_cast<float4*>(Wr + cc) = w;
+      for (int cb = lane * 4; cb < C; cb += 4 * 128) {
+        float4 v[4], w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 128;
+          if (cc < C) {
+            v[u] = *reinterpret_cast<const float4*>(Vr + cc);
+            w[u] = *reinterpret_cast<const float4*>(Wr + cc);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = cb + u * 128;
+          if (cc < C) {
+            float4 o;
+            o.x = w[u].x * p.decay - k * v[u].x;
+            o.y = w[u].y * p.decay - k * v[u].y;
+            o.z = w[u].z * p.decay - k * v[u].z;
+            o.w = w[u].w * p.decay - k * v[u].w;
+            *reinterpret_cast<float4*>(Wr + cc) = o;
+          }
+        }
       }
     } else {
       for (int cc = lane; cc < C; cc += 32) Wr[cc] = Wr[cc] * p.decay - k * Vr[cc];
