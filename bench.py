@@ -33,10 +33,11 @@ sys.path.insert(0, ROOT)
 METRIC = "owner Muon step ms & NS TFLOP/s vs bf16 peak; RMNP/AdamW HBM GB/s"
 
 # DRAM bytes of one step's 15 Newton-Schulz launches on the GPT-2 Large table,
-# from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the four-layer
-# table scaled x9 by matrices (profiles/ns_gemm_pair_gpt2l_4layers_full.md).
-# Valid only for the kernel source it was measured on.
-NS_TRAFFIC = {"source_sha256_16": "adc0df84ce3d0526", "workload": "gpt2l", "bytes_per_ns_segment": 36.27e9}
+# from ncu (dram__bytes_read.sum + dram__bytes_write.sum, one pass) over the 15
+# NS launches of one step on the full table
+# (profiles/ns_gemm_pair_gpt2l_tensor_active.md).
+# Valid only for the kernel source and tile schedule it was measured on.
+NS_TRAFFIC = {"source_sha256_16": "1f2a4aa73726bb49", "workload": "gpt2l", "bytes_per_ns_segment": 36.31e9}
 UNIT = "TFLOP/s"
 
 

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define MO_ABI_VERSION 2
+#define MO_ABI_VERSION 3
 
 enum mo_status {
   MO_OK = 0,
@@ -167,6 +167,39 @@ int muon_owner_step_noalloc(const mo_matrix* tbl, int32_t n, const mo_muon_param
 
 /* Size in bytes of the scratch array muon_owner_step_noalloc uses. */
 size_t mo_static_scratch_bytes(void);
+
+/* A Muon step planned once for a fixed table, hyperparameters and workspace
+ * (no counterpart on the pages; for callers that capture their training step
+ * in a CUDA graph). muon_owner_step uploads its workspace header from host
+ * memory on every call, which a graph cannot replay safely; a plan uploads it
+ * once, and each step then enqueues only device work.
+ *  - mo_muon_plan_create: validates and plans like muon_owner_step, binds the
+ *    plan to `ws` (same size and alignment rules) and enqueues the header
+ *    upload on `stream` (from pageable memory: call it outside any stream
+ *    capture). Steps on other streams must be ordered after that upload.
+ *    *out is set only on MO_OK; n must be >= 1.
+ *  - mo_muon_plan_step: enqueues one Muon step on `stream`: a memset of the
+ *    step's counters and flags, then the launches of muon_owner_step. No
+ *    host-to-device copy and no planning, so it may be captured in a CUDA
+ *    graph and the graph replayed. It returns MO_ERR_BAD_PARAM if the current
+ *    device is not the plan's. Results are bit-identical to muon_owner_step
+ *    with the same learning rate.
+ *  - Learning rate: every step reads lr from the device fp32 at
+ *    mo_muon_plan_lr_ptr(plan), initialised to params->lr by the create call,
+ *    so a schedule can write it between steps or graph replays (stream
+ *    ordered); decay = 1 - lr wd is formed on the device in double. The other
+ *    hyperparameters are fixed at creation.
+ *  - While a plan exists, `ws` belongs to it; two steps of one plan must not
+ *    be in flight at once. W, G and V are accessed through the table's
+ *    pointers, which must stay valid while steps or captured graphs run.
+ *  - mo_muon_plan_destroy frees host memory only; a graph captured from the
+ *    plan stays valid as long as `ws` and the tensors do. NULL is a no-op. */
+typedef struct mo_muon_plan_s* mo_muon_plan;
+int mo_muon_plan_create(const mo_matrix* tbl, int32_t n, const mo_muon_params* params,
+                        void* ws, size_t ws_bytes, cudaStream_t stream, mo_muon_plan* out);
+int mo_muon_plan_step(mo_muon_plan plan, cudaStream_t stream);
+float* mo_muon_plan_lr_ptr(mo_muon_plan plan);   /* device address; NULL for a NULL plan */
+int mo_muon_plan_destroy(mo_muon_plan plan);
 
 /* AdamW over every tail segment, on `stream` (one grouped launch per 256
  * segments). */

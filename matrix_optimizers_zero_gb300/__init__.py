@@ -140,6 +140,10 @@ def load_library() -> ctypes.CDLL:
         "mo_rmnp_colcut_workspace_bytes": (SZ, [P, I32]),
         "rmnp_colcut_step": (ctypes.c_int, [P, P, P, I32, P, P, SZ, P]),
         "mo_static_scratch_bytes": (SZ, []),
+        "mo_muon_plan_create": (ctypes.c_int, [P, I32, P, P, SZ, P, P]),
+        "mo_muon_plan_step": (ctypes.c_int, [P, P]),
+        "mo_muon_plan_lr_ptr": (P, [P]),
+        "mo_muon_plan_destroy": (ctypes.c_int, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -269,6 +273,41 @@ def muon_owner_step_noalloc(mats, params: Optional[MuonParams] = None, stream=No
 
 def mo_static_scratch_bytes() -> int:
     return int(load_library().mo_static_scratch_bytes())
+
+
+class MuonPlan:
+    """A Muon step planned once (mo_muon_plan_create): step() enqueues device
+    work only, so it can be captured in a CUDA graph and replayed. The
+    workspace belongs to the plan while it exists. `lr` is a one-element fp32
+    device tensor viewing the learning rate every step reads; write it (for
+    example with lr.fill_()) to follow a schedule between steps or replays."""
+
+    def __init__(self, mats, params: Optional[MuonParams] = None, workspace=None, stream=None):
+        import torch
+        self.table = _as_table(mats)
+        self.params = params or MuonParams()
+        self.workspace = workspace if workspace is not None else muon_workspace(self.table, self.params)
+        lib = load_library()
+        handle = ctypes.c_void_p()
+        st = lib.mo_muon_plan_create(self.table.ptr, self.table.n, ctypes.byref(self.params),
+                                     self.workspace.data_ptr(),
+                                     self.workspace.numel() * self.workspace.element_size(),
+                                     _stream_ptr(stream), ctypes.byref(handle))
+        _check(st, "mo_muon_plan_create")
+        self._handle = handle
+        lr_off = lib.mo_muon_plan_lr_ptr(handle) - self.workspace.data_ptr()
+        self.lr = self.workspace[lr_off:lr_off + 4].view(torch.float32)
+
+    def step(self, stream=None) -> None:
+        _check(load_library().mo_muon_plan_step(self._handle, _stream_ptr(stream)), "mo_muon_plan_step")
+
+    def close(self) -> None:
+        if self._handle is not None and _lib is not None:
+            _lib.mo_muon_plan_destroy(self._handle)
+        self._handle = None
+
+    def __del__(self):
+        self.close()
 
 
 # ---------------------------------------------------------------- RMNP / AdamW

@@ -101,26 +101,31 @@ void free_entry(PlanEntry* e) {
   delete e;
 }
 
-// Binds a planned layout to `ws` and builds the header image.
-int build_entry(PlanEntry& E, const mo_matrix* tbl, int32_t n, void* ws) {
-  mo::MuonLayout& L = E.L;
+// Binds a planned layout to `ws` and builds its header image.
+int bind_header(mo::MuonLayout& L, int32_t n, void* ws, std::vector<uint8_t>& header) {
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  E.header.assign(L.header_bytes, 0);
+  header.assign(L.header_bytes, 0);
   for (int32_t i = 0; i < n; ++i) {
     mo::DevMat& d = L.mats[size_t(i)];
     d.X[0] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[0]));
     d.X[1] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[1]));
     d.A = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.A));
     d.B = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.B));
-    if (!mo::encode_matrix_maps(d, L.ns_form, E.header.data() + L.off_tmaps + size_t(i) * mo::kMapsPerMat * mo::kTensorMapBytes))
+    if (!mo::encode_matrix_maps(d, L.ns_form, header.data() + L.off_tmaps + size_t(i) * mo::kMapsPerMat * mo::kTensorMapBytes))
       return cuda_fail(cudaErrorInvalidValue);
   }
-  std::memcpy(E.header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * size_t(n));
-  std::memcpy(E.header.data() + L.off_seg_prefix, L.seg_prefix.data(), sizeof(int64_t) * L.seg_prefix.size());
-  std::memcpy(E.header.data() + L.off_seg_code, L.seg_code.data(), sizeof(int32_t) * L.seg_code.size());
+  std::memcpy(header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * size_t(n));
+  std::memcpy(header.data() + L.off_seg_prefix, L.seg_prefix.data(), sizeof(int64_t) * L.seg_prefix.size());
+  std::memcpy(header.data() + L.off_seg_code, L.seg_code.data(), sizeof(int32_t) * L.seg_code.size());
   for (int ph = 0; ph < 3; ++ph)
     if (!L.tiles[ph].empty())
-      std::memcpy(E.header.data() + L.off_tiles[ph], L.tiles[ph].data(), sizeof(mo::TileRec) * L.tiles[ph].size());
+      std::memcpy(header.data() + L.off_tiles[ph], L.tiles[ph].data(), sizeof(mo::TileRec) * L.tiles[ph].size());
+  return MO_OK;
+}
+
+int build_entry(PlanEntry& E, const mo_matrix* tbl, int32_t n, void* ws) {
+  const int st = bind_header(E.L, n, ws, E.header);
+  if (st != MO_OK) return st;
   E.table.assign(tbl, tbl + n);
   E.ws = reinterpret_cast<uintptr_t>(ws);
   return MO_OK;
@@ -164,6 +169,9 @@ int insert_plan(PlanEntry* e, const mo_matrix* tbl, int32_t n, void* ws, bool wa
 }  // namespace
 
 namespace mo {
+
+int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* prm, const float* lr_dev,
+                 DeviceInfo* dev, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end);
 
 int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* ws, size_t ws_bytes,
                    cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end, bool allow_pinned) {
@@ -224,6 +232,14 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   if (e != cudaSuccess) return cuda_fail(e);
   if (use_pinned && (e = cudaEventRecord(E->uploaded, stream)) != cudaSuccess) return cuda_fail(e);
 
+  return enqueue_muon(L, wsb, prm, nullptr, dev, stream, ev_begin, ev_end);
+}
+
+// The prologue and Newton-Schulz launches of one step whose workspace header
+// is in place; the learning rate comes from `lr_dev` when it is set.
+int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* prm, const float* lr_dev,
+                 DeviceInfo* dev, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
+  cudaError_t e;
   const mo::DevMat* d_mats = reinterpret_cast<const mo::DevMat*>(wsb + L.off_meta);
   float* d_scales = reinterpret_cast<float*>(wsb + L.off_scales);
 
@@ -254,7 +270,8 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   np.b = prm->b;
   np.c = prm->c;
   np.lr = prm->lr;
-  np.decay = float(1.0 - double(prm->lr) * double(prm->wd));
+  np.wd = prm->wd;
+  np.lr_dev = lr_dev;
   np.lr_adjust = prm->lr_adjust;
   np.timeout_ns = 2000000000ull;
   // Launch kinds of one iteration and the tile schedule each one uses.
@@ -342,7 +359,80 @@ namespace mo {
 void note_cuda_error(int e) { t_last_cuda_error = e; }
 }  // namespace mo
 
+// A Muon step planned once: the layout bound to its workspace (header
+// uploaded at creation) and the hyperparameters.
+struct mo_muon_plan_s {
+  int dev = -1;
+  mo::MuonLayout L;
+  mo_muon_params params{};
+  uint8_t* ws = nullptr;
+};
+
 extern "C" {
+
+int mo_muon_plan_create(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws, size_t ws_bytes,
+                        cudaStream_t stream, mo_muon_plan* out) {
+  if (!out) return MO_ERR_NULL_POINTER;
+  int st = mo::validate_muon_params(params);
+  if (st != MO_OK) return st;
+  if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
+  if (n == 0) return MO_ERR_BAD_SHAPE;
+  if (!ws) return MO_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MO_ERR_MISALIGNED;
+  mo_muon_plan_s* P = new mo_muon_plan_s();
+  mo::plan_muon(tbl, n, mo::kBM, params->ns_form, P->L);
+  if (ws_bytes < P->L.total_bytes) {
+    delete P;
+    return MO_ERR_WORKSPACE_TOO_SMALL;
+  }
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MO_OK || cudaGetDevice(&P->dev) != cudaSuccess) {
+    delete P;
+    return st != MO_OK ? st : cuda_fail(cudaErrorInvalidDevice);
+  }
+  mo::order_prologue(P->L, int64_t(mo::kPrologueCtasPerSm) * dev->sms);
+  std::vector<uint8_t> header;
+  if ((st = bind_header(P->L, n, ws, header)) != MO_OK) {
+    delete P;
+    return st;
+  }
+  std::memcpy(header.data() + P->L.off_lr, &params->lr, sizeof(float));
+  // pageable source: the copy is staged before cudaMemcpyAsync returns
+  const cudaError_t e = cudaMemcpyAsync(ws, header.data(), P->L.header_bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) {
+    delete P;
+    return cuda_fail(e);
+  }
+  P->params = *params;
+  P->ws = static_cast<uint8_t*>(ws);
+  *out = P;
+  return MO_OK;
+}
+
+int mo_muon_plan_step(mo_muon_plan plan, cudaStream_t stream) {
+  if (!plan) return MO_ERR_NULL_POINTER;
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != MO_OK) return st;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->dev) return MO_ERR_BAD_PARAM;
+  const mo::MuonLayout& L = plan->L;
+  // the prologue's counters and flags start from zero (a per-call upload
+  // would have reset them; a step that gave up may have left them set)
+  cudaError_t e = cudaMemsetAsync(plan->ws + L.off_counters, 0, L.off_lr - L.off_counters, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return mo::enqueue_muon(L, plan->ws, &plan->params, reinterpret_cast<const float*>(plan->ws + L.off_lr), dev,
+                          stream, nullptr, nullptr);
+}
+
+float* mo_muon_plan_lr_ptr(mo_muon_plan plan) {
+  return plan ? reinterpret_cast<float*>(plan->ws + plan->L.off_lr) : nullptr;
+}
+
+int mo_muon_plan_destroy(mo_muon_plan plan) {
+  delete plan;
+  return MO_OK;
+}
 
 size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_params* params) {
   if (mo::validate_muon_params(params) != MO_OK) return 0;

@@ -20,7 +20,8 @@ struct NsParams {
   int32_t cur;                // X buffer read by this launch
   float a, b, c;
   float lr;
-  float decay;                // 1 - lr wd, rounded once from double on the host
+  float wd;
+  const float* lr_dev;        // when set, the learning rate is read from this device float instead of `lr`
   int32_t lr_adjust;          // mo_lr_adjust: which per-matrix scale the update uses
   uint64_t timeout_ns;
 };

@@ -174,7 +174,7 @@ __device__ __forceinline__ void epilogue_symmetric(const NsParams& p, const DevM
 }
 
 // UPDATE: X' = a X + acc (bf16 to the other X buffer), or in the last
-// iteration W <- W decay - lr s X' on the stored orientation.
+// iteration W <- W decay - lr s X' on the stored orientation (decay = 1 - lr wd).
 template <int PHASE, bool LAST>
 __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat& M, int row, int cbase,
                                                 uint32_t tb) {
@@ -228,8 +228,10 @@ __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat&
           if (col0 + i < n) o_row[i] = float_to_bf16_bits(v[i]);
       }
     } else {
-      const float decay = p.decay;
-      const float step = p.lr * (p.lr_adjust == MO_LR_MATCH_RMS_ADAMW ? M.rms_scale : M.shape_scale);
+      const float lr = p.lr_dev != nullptr ? *p.lr_dev : p.lr;
+      // 1 - lr wd, rounded once from double (explicit roundings: no contraction)
+      const float decay = float(__dsub_rn(1.0, __dmul_rn(double(lr), double(p.wd))));
+      const float step = lr * (p.lr_adjust == MO_LR_MATCH_RMS_ADAMW ? M.rms_scale : M.shape_scale);
       // W is read and written once here: evict-first keeps the operand
       // panels the main loop re-reads in L2 (measured: 0.7 GB less DRAM
       // traffic and ~4% off this launch on the GPT-2 Large table)

@@ -237,6 +237,8 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout&
   off = align_up(off + sizeof(uint32_t) * size_t(n), 256);
   L.off_abort = off;
   off = align_up(off + sizeof(uint32_t), 256);
+  L.off_lr = off;
+  off = align_up(off + sizeof(float), 256);
   for (int ph = 0; ph < 3; ++ph) {
     L.off_tiles[ph] = off;
     off = align_up(off + sizeof(TileRec) * L.tiles[ph].size(), 256);

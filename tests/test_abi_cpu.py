@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
     assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.mo_abi_version() == 2
+    assert lib.mo_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -172,6 +172,33 @@ def test_muon_validation_codes(lib):
     assert _muon(lib, ok, 1, p, ws_bytes=1024) == -5
     big = mo.fake_table([(70000, 70000)])
     assert _muon(lib, big, 1, p) == -2                          # m above the supported maximum
+
+
+def test_muon_plan_validation_codes(lib):
+    """mo_muon_plan_create rejects bad arguments before any CUDA call; the
+    other plan entry points accept NULL plans."""
+    p = mo.MuonParams()
+    ok = mo.fake_table([(16, 32)])
+    out = ctypes.c_void_p()
+
+    def create(arr, n, params=p, ws=1 << 30, ws_bytes=1 << 40, out_ptr=ctypes.byref(out)):
+        return lib.mo_muon_plan_create(ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None, n,
+                                       ctypes.byref(params), ws, ws_bytes, None, out_ptr)
+
+    assert create(ok, 1, out_ptr=None) == -1
+    assert create(None, 1) == -1
+    assert create(None, 0) == -2                     # a plan needs at least one matrix
+    assert create(ok, 1, params=mo.MuonParams(ns_steps=0)) == -4
+    assert create(ok, 1, ws=0) == -1
+    assert create(ok, 1, ws=(1 << 30) + 16) == -3
+    assert create(ok, 1, ws_bytes=1024) == -5
+    mis = mo.fake_table([(16, 32)])
+    mis[0].W += 4
+    assert create(mis, 1) == -3
+    assert out.value is None                         # never set on failure
+    assert lib.mo_muon_plan_step(None, None) == -1
+    assert lib.mo_muon_plan_lr_ptr(None) is None
+    assert lib.mo_muon_plan_destroy(None) == 0
 
 
 def test_adamw_and_rmnp_validation_codes(lib):
