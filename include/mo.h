@@ -231,6 +231,28 @@ int rmnp_step_scaled(const mo_matrix* tbl, const float* scales, int32_t n,
  * (MO_ERR_BAD_PARAM otherwise). */
 int htrmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, float power, cudaStream_t stream);
 
+/* Device-resident hyperparameters, for steps captured in a CUDA graph (no
+ * counterpart on the pages). A captured launch keeps the arguments it was
+ * captured with; these entry points read the values that change from step to
+ * step from device memory when the kernels run, so a schedule can update them
+ * between replays (stream ordered).
+ *  - adamw_tail_step_dev: as adamw_tail_step, with t (after the increment,
+ *    >= 1) read from the device int64 *d_step (8-byte aligned), and lr from
+ *    the device float *d_lr when d_lr is not NULL (4-byte aligned). The
+ *    caller advances *d_step between steps (for example inside the captured
+ *    graph); params->step, and params->lr when d_lr is set, are ignored (and
+ *    not validated). The device values are used as found.
+ *  - rmnp_step_dev: rmnp_step (power 0) or htrmnp_step (power in (0, 1]),
+ *    with lr read from the device float *d_lr (not NULL); params->lr is
+ *    ignored.
+ * Every AdamW and RMNP kernel forms its per-step factors (1 - lr wd, the
+ * bias corrections) on the device from lr, wd and t, so these entry points
+ * give results bit-identical to the by-value ones for the same values. */
+int adamw_tail_step_dev(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* params,
+                        const int64_t* d_step, const float* d_lr, cudaStream_t stream);
+int rmnp_step_dev(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, float power,
+                  const float* d_lr, cudaStream_t stream);
+
 /* RMNP with rows cut into column shards ("Optimizers In A Sharded World",
  * section 3, column-cut tensor parallelism, and the appendix's column-cut
  * scheme), evaluated on one GPU: each table entry is one dense column shard

@@ -140,6 +140,8 @@ def load_library() -> ctypes.CDLL:
         "mo_rmnp_colcut_workspace_bytes": (SZ, [P, I32]),
         "rmnp_colcut_step": (ctypes.c_int, [P, P, P, I32, P, P, SZ, P]),
         "mo_static_scratch_bytes": (SZ, []),
+        "adamw_tail_step_dev": (ctypes.c_int, [P, I32, P, P, P, P]),
+        "rmnp_step_dev": (ctypes.c_int, [P, I32, P, ctypes.c_float, P, P]),
         "mo_muon_plan_create": (ctypes.c_int, [P, I32, P, P, SZ, P, P]),
         "mo_muon_plan_step": (ctypes.c_int, [P, P]),
         "mo_muon_plan_lr_ptr": (P, [P]),
@@ -329,6 +331,17 @@ def htrmnp_step(mats, params: Optional[RmnpParams] = None, power: float = HTRMNP
            "htrmnp_step")
 
 
+def rmnp_step_dev(mats, params, lr, power: float = 0.0, stream=None) -> None:
+    """rmnp_step (power 0) or htrmnp_step with lr read from the one-element
+    fp32 CUDA tensor `lr` when the kernels run (capturable in a CUDA graph)."""
+    import torch
+    t = _as_table(mats)
+    if lr.dtype != torch.float32 or lr.numel() != 1 or not lr.is_cuda:
+        raise TypeError("lr must be a one-element fp32 CUDA tensor")
+    _check(load_library().rmnp_step_dev(t.ptr, t.n, ctypes.byref(params), float(power), lr.data_ptr(),
+                                        _stream_ptr(stream)), "rmnp_step_dev")
+
+
 def rmnp_step_scaled(mats, scales: Sequence[float], params: Optional[RmnpParams] = None, stream=None) -> None:
     t = _as_table(mats)
     params = params or RmnpParams()
@@ -363,6 +376,21 @@ def adamw_tail_step(segs, params: Optional[AdamWParams] = None, stream=None) -> 
     params = params or AdamWParams()
     _check(load_library().adamw_tail_step(t.ptr, t.n, ctypes.byref(params), _stream_ptr(stream)),
            "adamw_tail_step")
+
+
+def adamw_tail_step_dev(segs, params, step, lr=None, stream=None) -> None:
+    """adamw_tail_step with t read from the one-element int64 CUDA tensor
+    `step` (after the increment) and, if given, lr from the one-element fp32
+    CUDA tensor `lr`, when the kernel runs (capturable in a CUDA graph)."""
+    import torch
+    t = segs if isinstance(segs, TailTable) else TailTable(segs)
+    if step.dtype != torch.int64 or step.numel() != 1 or not step.is_cuda:
+        raise TypeError("step must be a one-element int64 CUDA tensor")
+    if lr is not None and (lr.dtype != torch.float32 or lr.numel() != 1 or not lr.is_cuda):
+        raise TypeError("lr must be a one-element fp32 CUDA tensor")
+    _check(load_library().adamw_tail_step_dev(t.ptr, t.n, ctypes.byref(params), step.data_ptr(),
+                                              lr.data_ptr() if lr is not None else None, _stream_ptr(stream)),
+           "adamw_tail_step_dev")
 
 
 # ---------------------------------------------------------------- diagnostics

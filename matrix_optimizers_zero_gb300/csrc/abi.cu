@@ -300,7 +300,7 @@ int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* pr
 namespace {
 
 int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmnp_params* prm, float power,
-              cudaStream_t stream) {
+              const float* lr_dev, cudaStream_t stream) {
   int st = mo::validate_rmnp_params(prm);
   if (st != MO_OK) return st;
   if (!std::isfinite(power) || power < 0.f || power > 1.f) return MO_ERR_BAD_PARAM;
@@ -319,8 +319,9 @@ int rmnp_impl(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmn
     int32_t b = 0;
     while (b < n) {
       std::memset(&rp, 0, sizeof(rp));
-      rp.decay = float(1.0 - double(prm->lr) * double(prm->wd));
       rp.lr = prm->lr;
+      rp.wd = prm->wd;
+      rp.lr_dev = lr_dev;
       rp.mu = prm->mu;
       rp.eps = prm->eps;
       rp.power = power;
@@ -367,6 +368,49 @@ struct mo_muon_plan_s {
   mo_muon_params params{};
   uint8_t* ws = nullptr;
 };
+
+namespace {
+
+// AdamW over the segments; t and lr by value, or from device memory when
+// step_dev / lr_dev are set (the kernel forms the per-step factors either way).
+int adamw_impl(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* params, const int64_t* step_dev,
+               const float* lr_dev, cudaStream_t stream) {
+  DeviceInfo* dev = nullptr;
+  const int st = device_info(&dev);
+  if (st != MO_OK) return st;
+  static thread_local mo::AdamParams ap;
+  int32_t i = 0;
+  while (i < n) {
+    std::memset(&ap, 0, sizeof(ap));
+    ap.lr = params->lr;
+    ap.wd = params->wd;
+    ap.step = params->step;
+    ap.lr_dev = lr_dev;
+    ap.step_dev = step_dev;
+    ap.beta1 = params->beta1;
+    ap.beta2 = params->beta2;
+    ap.eps = params->eps;
+    int32_t cnt = 0;
+    int64_t items = 0;
+    for (; i < n && cnt < mo::kAdamMaxSegs; ++i) {
+      const mo_tail_seg& s = segs[i];
+      if (s.numel == 0) continue;
+      ap.s[cnt] = mo::AdamSeg{s.p, s.g, s.m, s.v, s.numel};
+      ap.item_prefix[cnt] = items;
+      items += (s.numel + mo::kAdamItem - 1) / mo::kAdamItem;
+      ++cnt;
+    }
+    ap.item_prefix[cnt] = items;
+    ap.n = cnt;
+    if (cnt == 0) break;
+    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items, int64_t(dev->sms) * 8)));
+    cudaError_t e = mo::launch_adamw(ap, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return MO_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -454,17 +498,26 @@ int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params*
 }
 
 int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cudaStream_t stream) {
-  return rmnp_impl(tbl, nullptr, n, params, 0.0f, stream);
+  return rmnp_impl(tbl, nullptr, n, params, 0.0f, nullptr, stream);
 }
 
 int rmnp_step_scaled(const mo_matrix* tbl, const float* scales, int32_t n, const mo_rmnp_params* params,
                      cudaStream_t stream) {
   if (n > 0 && !scales) return MO_ERR_NULL_POINTER;
-  return rmnp_impl(tbl, scales, n, params, 0.0f, stream);
+  return rmnp_impl(tbl, scales, n, params, 0.0f, nullptr, stream);
 }
 
 int htrmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, float power, cudaStream_t stream) {
-  return rmnp_impl(tbl, nullptr, n, params, power, stream);
+  return rmnp_impl(tbl, nullptr, n, params, power, nullptr, stream);
+}
+
+int rmnp_step_dev(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, float power, const float* d_lr,
+                  cudaStream_t stream) {
+  if (!d_lr || !params) return MO_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(d_lr) & 3u) != 0) return MO_ERR_MISALIGNED;
+  mo_rmnp_params q = *params;   // lr comes from device memory
+  q.lr = 0.0f;
+  return rmnp_impl(tbl, nullptr, n, &q, power, d_lr, stream);
 }
 
 size_t mo_rmnp_colcut_workspace_bytes(const mo_matrix* shards, int32_t n) {
@@ -497,8 +550,8 @@ int rmnp_colcut_step(const mo_matrix* shards, const int32_t* group, const float*
   static thread_local mo::ColcutParams cp;
   std::memset(&cp, 0, sizeof(cp));
   cp.n = n;
-  cp.decay = float(1.0 - double(params->lr) * double(params->wd));
   cp.lr = params->lr;
+  cp.wd = params->wd;
   cp.mu = params->mu;
   cp.eps = params->eps;
   cp.partials = static_cast<float*>(ws);
@@ -528,43 +581,28 @@ int rmnp_colcut_step(const mo_matrix* shards, const int32_t* group, const float*
   return MO_OK;
 }
 
+
 int adamw_tail_step(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* params, cudaStream_t stream) {
-  int st = mo::validate_adamw(segs, n, params);
+  const int st = mo::validate_adamw(segs, n, params);
   if (st != MO_OK) return st;
   if (n == 0) return MO_OK;
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != MO_OK) return st;
-  const double t = double(params->step);
-  const double bc1 = 1.0 - std::pow(double(params->beta1), t);
-  const double bc2 = 1.0 - std::pow(double(params->beta2), t);
-  static thread_local mo::AdamParams ap;
-  int32_t i = 0;
-  while (i < n) {
-    std::memset(&ap, 0, sizeof(ap));
-    ap.decay = float(1.0 - double(params->lr) * double(params->wd));
-    ap.step_size = float(double(params->lr) / bc1);
-    ap.inv_bc2_sqrt = float(1.0 / std::sqrt(bc2));
-    ap.beta1 = params->beta1;
-    ap.beta2 = params->beta2;
-    ap.eps = params->eps;
-    int32_t cnt = 0;
-    int64_t items = 0;
-    for (; i < n && cnt < mo::kAdamMaxSegs; ++i) {
-      const mo_tail_seg& s = segs[i];
-      if (s.numel == 0) continue;
-      ap.s[cnt] = mo::AdamSeg{s.p, s.g, s.m, s.v, s.numel};
-      ap.item_prefix[cnt] = items;
-      items += (s.numel + mo::kAdamItem - 1) / mo::kAdamItem;
-      ++cnt;
-    }
-    ap.item_prefix[cnt] = items;
-    ap.n = cnt;
-    if (cnt == 0) break;
-    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items, int64_t(dev->sms) * 8)));
-    cudaError_t e = mo::launch_adamw(ap, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
-  return MO_OK;
+  return adamw_impl(segs, n, params, nullptr, nullptr, stream);
+}
+
+int adamw_tail_step_dev(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* params, const int64_t* d_step,
+                        const float* d_lr, cudaStream_t stream) {
+  if (!params) return MO_ERR_NULL_POINTER;
+  mo_adamw_params q = *params;   // the values read from device memory are not validated here
+  q.step = 1;
+  if (d_lr) q.lr = 0.0f;
+  const int st = mo::validate_adamw(segs, n, &q);
+  if (st != MO_OK) return st;
+  params = &q;
+  if (!d_step) return MO_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(d_step) & 7u) != 0 || (reinterpret_cast<uintptr_t>(d_lr) & 3u) != 0)
+    return MO_ERR_MISALIGNED;
+  if (n == 0) return MO_OK;
+  return adamw_impl(segs, n, params, d_step, d_lr, stream);
 }
 
 int mo_last_device_error(cudaStream_t stream) {

@@ -46,6 +46,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   return false;
 }
 
+// 1 - lr wd, rounded once from double with explicit roundings (no
+// contraction into a fused multiply-add). Every kernel forms the decoupled
+// weight decay this way from lr and wd, whether they arrive by value or from
+// device memory, so the two kinds of entry point agree bit for bit.
+__device__ __forceinline__ float decay_factor(float lr, float wd) {
+  return float(__dsub_rn(1.0, __dmul_rn(double(lr), double(wd))));
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }

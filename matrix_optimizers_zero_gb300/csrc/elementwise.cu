@@ -318,9 +318,9 @@ __global__ void __launch_bounds__(256, kPrologueCtasPerSm) muon_prologue_kernel(
 // lr s / max(||V_i||, eps) for RMNP; lr s max(||V_i||, eps)^(power - 1) for
 // HTRMNP (a reading of "Optimizers In A Sharded World" section 7, which names
 // the power scaling without printing a formula).
-__device__ __forceinline__ float rmnp_factor(const RmnpParams& p, float scale, float sum_sq) {
+__device__ __forceinline__ float rmnp_factor(const RmnpParams& p, float lr, float scale, float sum_sq) {
   const float nrm = fmaxf(sqrtf(sum_sq), p.eps);
-  return p.power == 0.0f ? p.lr * scale / nrm : p.lr * scale * powf(nrm, p.power - 1.0f);
+  return p.power == 0.0f ? lr * scale / nrm : lr * scale * powf(nrm, p.power - 1.0f);
 }
 //
 // One warp per stored row ("Optimizers In A Sharded World", section 1 and the
@@ -330,6 +330,8 @@ __device__ __forceinline__ float rmnp_factor(const RmnpParams& p, float scale, f
 // result does not depend on which other rows share the launch); pass 2 re-reads
 // V_i (just written, served from L2) and updates W_i.
 __global__ void __launch_bounds__(256) rmnp_kernel(const __grid_constant__ RmnpParams p) {
+  const float lr = p.lr_dev != nullptr ? *p.lr_dev : p.lr;
+  const float decay = decay_factor(lr, p.wd);
   const int lane = int(threadIdx.x & 31);
   const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(256) rmnp_kernel(const __grid_constant__ RmnpP
       }
     }
     ss = warp_sum(ss);
-    const float k = rmnp_factor(p, E.scale, ss);
+    const float k = rmnp_factor(p, lr, E.scale, ss);
     if (E.vec_ok) {
       for (int cb = lane * 4; cb < C; cb += 4 * 128) {
         float4 v[4], w[4];
@@ -401,16 +403,16 @@ __global__ void __launch_bounds__(256) rmnp_kernel(const __grid_constant__ RmnpP
           const int cc = cb + u * 128;
           if (cc < C) {
             float4 o;
-            o.x = w[u].x * p.decay - k * v[u].x;
-            o.y = w[u].y * p.decay - k * v[u].y;
-            o.z = w[u].z * p.decay - k * v[u].z;
-            o.w = w[u].w * p.decay - k * v[u].w;
+            o.x = w[u].x * decay - k * v[u].x;
+            o.y = w[u].y * decay - k * v[u].y;
+            o.z = w[u].z * decay - k * v[u].z;
+            o.w = w[u].w * decay - k * v[u].w;
             *reinterpret_cast<float4*>(Wr + cc) = o;
           }
         }
       }
     } else {
-      for (int cc = lane; cc < C; cc += 32) Wr[cc] = Wr[cc] * p.decay - k * Vr[cc];
+      for (int cc = lane; cc < C; cc += 32) Wr[cc] = Wr[cc] * decay - k * Vr[cc];
     }
   }
 }
@@ -422,6 +424,8 @@ __global__ void __launch_bounds__(256) rmnp_kernel(const __grid_constant__ RmnpP
 // strided sums, a fixed xor tree per warp, the 8 warps in order), so a row's
 // result does not depend on the launch either.
 __global__ void __launch_bounds__(256) rmnp_row_cta_kernel(const __grid_constant__ RmnpParams p) {
+  const float lr = p.lr_dev != nullptr ? *p.lr_dev : p.lr;
+  const float decay = decay_factor(lr, p.wd);
   __shared__ float red[8];
   const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
   const int64_t total = p.row_prefix[p.n];
@@ -481,7 +485,7 @@ __global__ void __launch_bounds__(256) rmnp_row_cta_kernel(const __grid_constant
 #pragma unroll
     for (int w = 0; w < 8; ++w) tot += red[w];
     __syncthreads();   // red is rewritten by the next row
-    const float k = rmnp_factor(p, E.scale, tot);
+    const float k = rmnp_factor(p, lr, E.scale, tot);
     if (E.vec_ok) {
       for (int cb = tid * 4; cb < C; cb += 4 * 1024) {
         float4 v[4], w[4];
@@ -498,16 +502,16 @@ __global__ void __launch_bounds__(256) rmnp_row_cta_kernel(const __grid_constant
           const int cc = cb + u * 1024;
           if (cc < C) {
             float4 o;
-            o.x = w[u].x * p.decay - k * v[u].x;
-            o.y = w[u].y * p.decay - k * v[u].y;
-            o.z = w[u].z * p.decay - k * v[u].z;
-            o.w = w[u].w * p.decay - k * v[u].w;
+            o.x = w[u].x * decay - k * v[u].x;
+            o.y = w[u].y * decay - k * v[u].y;
+            o.z = w[u].z * decay - k * v[u].z;
+            o.w = w[u].w * decay - k * v[u].w;
             *reinterpret_cast<float4*>(Wr + cc) = o;
           }
         }
       }
     } else {
-      for (int cc = tid; cc < C; cc += 256) Wr[cc] = Wr[cc] * p.decay - k * Vr[cc];
+      for (int cc = tid; cc < C; cc += 256) Wr[cc] = Wr[cc] * decay - k * Vr[cc];
     }
   }
 }
@@ -586,6 +590,7 @@ __global__ void __launch_bounds__(256) colcut_partial_kernel(const __grid_consta
 }
 
 __global__ void __launch_bounds__(256) colcut_apply_kernel(const __grid_constant__ ColcutParams p) {
+  const float decay = decay_factor(p.lr, p.wd);
   const int lane = int(threadIdx.x & 31);
   const int64_t gw = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (int64_t(gridDim.x) * blockDim.x) >> 5;
@@ -617,16 +622,16 @@ __global__ void __launch_bounds__(256) colcut_apply_kernel(const __grid_constant
           const int cc = cb + u * 128;
           if (cc < C) {
             float4 o;
-            o.x = w[u].x * p.decay - k * v[u].x;
-            o.y = w[u].y * p.decay - k * v[u].y;
-            o.z = w[u].z * p.decay - k * v[u].z;
-            o.w = w[u].w * p.decay - k * v[u].w;
+            o.x = w[u].x * decay - k * v[u].x;
+            o.y = w[u].y * decay - k * v[u].y;
+            o.z = w[u].z * decay - k * v[u].z;
+            o.w = w[u].w * decay - k * v[u].w;
             *reinterpret_cast<float4*>(Wr + cc) = o;
           }
         }
       }
     } else {
-      for (int cc = lane; cc < C; cc += 32) Wr[cc] = Wr[cc] * p.decay - k * Vr[cc];
+      for (int cc = lane; cc < C; cc += 32) Wr[cc] = Wr[cc] * decay - k * Vr[cc];
     }
   }
 }
@@ -636,14 +641,39 @@ __global__ void __launch_bounds__(256) colcut_apply_kernel(const __grid_constant
 // Decoupled AdamW with bias correction on the packed tail ("MatrixFSDP",
 // sections 3 and 5.1). Work items of 4096 elements; each thread handles four
 // 16-byte vectors per item, loads issued before use.
-__device__ __forceinline__ void adam_elem(const AdamParams& p, float& pp, float g, float& m, float& v) {
+// Per-step factors of AdamW, formed on the device from lr, wd and t (by
+// value, or read from device memory): decay 1 - lr wd, step size
+// lr / (1 - beta1^t) and 1 / sqrt(1 - beta2^t), each rounded once from double.
+struct AdamFactors {
+  float decay, step_size, inv_bc2_sqrt;
+};
+
+__device__ __forceinline__ AdamFactors adam_factors(const AdamParams& p) {
+  const float lr = p.lr_dev != nullptr ? *p.lr_dev : p.lr;
+  const double t = double(p.step_dev != nullptr ? *p.step_dev : p.step);
+  const double bc1 = 1.0 - pow(double(p.beta1), t);
+  const double bc2 = 1.0 - pow(double(p.beta2), t);
+  AdamFactors f;
+  f.decay = decay_factor(lr, p.wd);
+  f.step_size = float(double(lr) / bc1);
+  f.inv_bc2_sqrt = float(1.0 / sqrt(bc2));
+  return f;
+}
+
+__device__ __forceinline__ void adam_elem(const AdamParams& p, const AdamFactors& f, float& pp, float g, float& m,
+                                          float& v) {
   m = fmaf(p.beta1, m, (1.0f - p.beta1) * g);
   v = fmaf(p.beta2, v, (1.0f - p.beta2) * g * g);
-  const float denom = fmaf(sqrtf(v), p.inv_bc2_sqrt, p.eps);
-  pp = pp * p.decay - p.step_size * (m / denom);
+  const float denom = fmaf(sqrtf(v), f.inv_bc2_sqrt, p.eps);
+  pp = pp * f.decay - f.step_size * (m / denom);
 }
 
 __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ AdamParams p) {
+  // one thread forms the factors (double pow: slow FP64 units, so not per thread)
+  __shared__ AdamFactors sf;
+  if (threadIdx.x == 0) sf = adam_factors(p);
+  __syncthreads();
+  const AdamFactors f = sf;
   const int64_t total = p.item_prefix[p.n];
   for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
     int lo = 0, hi = p.n - 1;
@@ -670,17 +700,17 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
     for (int u = 0; u < 4; ++u) {
       const int64_t e = e0 + int64_t(u * 256 + int(threadIdx.x)) * 4;
       if (full[u]) {
-        adam_elem(p, P[u].x, G[u].x, Mm[u].x, Vv[u].x);
-        adam_elem(p, P[u].y, G[u].y, Mm[u].y, Vv[u].y);
-        adam_elem(p, P[u].z, G[u].z, Mm[u].z, Vv[u].z);
-        adam_elem(p, P[u].w, G[u].w, Mm[u].w, Vv[u].w);
+        adam_elem(p, f, P[u].x, G[u].x, Mm[u].x, Vv[u].x);
+        adam_elem(p, f, P[u].y, G[u].y, Mm[u].y, Vv[u].y);
+        adam_elem(p, f, P[u].z, G[u].z, Mm[u].z, Vv[u].z);
+        adam_elem(p, f, P[u].w, G[u].w, Mm[u].w, Vv[u].w);
         *reinterpret_cast<float4*>(S.p + e) = P[u];
         *reinterpret_cast<float4*>(S.m + e) = Mm[u];
         *reinterpret_cast<float4*>(S.v + e) = Vv[u];
       } else if (e < S.numel) {
         for (int64_t j = e; j < S.numel && j < e + 4; ++j) {
           float pp = S.p[j], mm = S.m[j], vv = S.v[j];
-          adam_elem(p, pp, S.g[j], mm, vv);
+          adam_elem(p, f, pp, S.g[j], mm, vv);
           S.p[j] = pp;
           S.m[j] = mm;
           S.v[j] = vv;

@@ -70,8 +70,9 @@ struct RmnpParams {
   RmnpEntry e[kRmnpMaxEntries];
   int64_t row_prefix[kRmnpMaxEntries + 1];
   int32_t n;
-  float decay, lr, mu, eps;
+  float lr, wd, mu, eps;
   float power;                // HTRMNP: rows scaled by max(||V_i||, eps)^(power - 1); 0 for RMNP
+  const float* lr_dev;        // when set, the learning rate is read from this device float instead of `lr`
 };
 // Rows of at least kRmnpLongRow elements go to the CTA-per-row kernel (its
 // grid: CTAs), the others to the warp-per-row kernel (grid: CTAs of 8 warps).
@@ -86,7 +87,7 @@ struct ColcutParams {
   int16_t last[kRmnpMaxEntries];
   float* partials;
   int32_t n;
-  float decay, lr, mu, eps;
+  float lr, wd, mu, eps;
 };
 cudaError_t launch_rmnp_colcut(const ColcutParams& p, int grid, cudaStream_t stream);
 
@@ -104,9 +105,10 @@ struct AdamParams {
   AdamSeg s[kAdamMaxSegs];
   int64_t item_prefix[kAdamMaxSegs + 1];
   int32_t n;
-  float decay;        // 1 - lr wd
-  float step_size;    // lr / (1 - beta1^t)
-  float inv_bc2_sqrt; // 1 / sqrt(1 - beta2^t)
+  float lr, wd;
+  int64_t step;              // t after the increment (>= 1)
+  const float* lr_dev;       // when set, lr is read from this device float
+  const int64_t* step_dev;   // when set, t is read from this device int64
   float beta1, beta2, eps;
 };
 cudaError_t launch_adamw(const AdamParams& p, int grid, cudaStream_t stream);

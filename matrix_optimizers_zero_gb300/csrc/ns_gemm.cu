@@ -229,8 +229,7 @@ __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat&
       }
     } else {
       const float lr = p.lr_dev != nullptr ? *p.lr_dev : p.lr;
-      // 1 - lr wd, rounded once from double (explicit roundings: no contraction)
-      const float decay = float(__dsub_rn(1.0, __dmul_rn(double(lr), double(p.wd))));
+      const float decay = decay_factor(lr, p.wd);
       const float step = lr * (p.lr_adjust == MO_LR_MATCH_RMS_ADAMW ? M.rms_scale : M.shape_scale);
       // W is read and written once here: evict-first keeps the operand
       // panels the main loop re-reads in L2 (measured: 0.7 GB less DRAM

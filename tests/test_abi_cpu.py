@@ -229,3 +229,27 @@ def test_adamw_and_rmnp_validation_codes(lib):
         assert lib.htrmnp_step(tp, 1, ctypes.byref(mo.RmnpParams()), ctypes.c_float(bad_power), None) == -4
     assert lib.htrmnp_step(None, 0, ctypes.byref(mo.RmnpParams()), ctypes.c_float(0.125), None) == 0
     assert lib.htrmnp_step(tp, 1, ctypes.byref(mo.RmnpParams(eps=-1.0)), ctypes.c_float(0.125), None) == -4
+
+
+def test_device_hyperparameter_validation_codes(lib):
+    """adamw_tail_step_dev / rmnp_step_dev: null or misaligned device
+    pointers are rejected before any CUDA call; the by-value fields they
+    replace are not validated."""
+    seg = (mo.MoTailSeg * 1)()
+    seg[0] = mo.MoTailSeg(1 << 20, 2 << 20, 3 << 20, 4 << 20, 1000)
+    sp = ctypes.cast(seg, ctypes.c_void_p)
+    step_ptr, lr_ptr = 5 << 20, 6 << 20
+    assert lib.adamw_tail_step_dev(sp, 1, ctypes.byref(mo.AdamWParams()), None, None, None) == -1
+    assert lib.adamw_tail_step_dev(sp, 1, ctypes.byref(mo.AdamWParams()), step_ptr + 4, None, None) == -3
+    assert lib.adamw_tail_step_dev(sp, 1, ctypes.byref(mo.AdamWParams()), step_ptr, lr_ptr + 2, None) == -3
+    assert lib.adamw_tail_step_dev(sp, 1, None, step_ptr, None, None) == -1
+    assert lib.adamw_tail_step_dev(sp, 1, ctypes.byref(mo.AdamWParams(beta1=1.0)), step_ptr, None, None) == -4
+    assert lib.adamw_tail_step_dev(None, 0, ctypes.byref(mo.AdamWParams(step=0)), step_ptr, None, None) == 0
+    t = mo.fake_table([(16, 32)])
+    tp = ctypes.cast(t, ctypes.c_void_p)
+    assert lib.rmnp_step_dev(tp, 1, ctypes.byref(mo.RmnpParams()), ctypes.c_float(0.0), None, None) == -1
+    assert lib.rmnp_step_dev(tp, 1, ctypes.byref(mo.RmnpParams()), ctypes.c_float(0.0), lr_ptr + 1, None) == -3
+    assert lib.rmnp_step_dev(tp, 1, ctypes.byref(mo.RmnpParams(eps=-1.0)), ctypes.c_float(0.0), lr_ptr, None) == -4
+    assert lib.rmnp_step_dev(tp, 1, ctypes.byref(mo.RmnpParams()), ctypes.c_float(2.0), lr_ptr, None) == -4
+    assert lib.rmnp_step_dev(None, 0, ctypes.byref(mo.RmnpParams(lr=float("nan"))), ctypes.c_float(0.0),
+                             lr_ptr, None) == 0
