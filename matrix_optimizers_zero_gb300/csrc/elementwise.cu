@@ -648,11 +648,23 @@ struct AdamFactors {
   float decay, step_size, inv_bc2_sqrt;
 };
 
+// b^e for e >= 0 by square-and-multiply (at most 2 log2(e) double products:
+// far shorter than a general power on the few FP64 units)
+__device__ __forceinline__ double pow_int(double b, int64_t e) {
+  double r = 1.0;
+  while (e > 0) {
+    if (e & 1) r = __dmul_rn(r, b);
+    b = __dmul_rn(b, b);
+    e >>= 1;
+  }
+  return r;
+}
+
 __device__ __forceinline__ AdamFactors adam_factors(const AdamParams& p) {
   const float lr = p.lr_dev != nullptr ? *p.lr_dev : p.lr;
-  const double t = double(p.step_dev != nullptr ? *p.step_dev : p.step);
-  const double bc1 = 1.0 - pow(double(p.beta1), t);
-  const double bc2 = 1.0 - pow(double(p.beta2), t);
+  const int64_t t = p.step_dev != nullptr ? *p.step_dev : p.step;
+  const double bc1 = 1.0 - pow_int(double(p.beta1), t);
+  const double bc2 = 1.0 - pow_int(double(p.beta2), t);
   AdamFactors f;
   f.decay = decay_factor(lr, p.wd);
   f.step_size = float(double(lr) / bc1);
