@@ -242,18 +242,23 @@ def run_ours(args, rank, world, local_rank):
     ws_ptr, ws_bytes = ws.data_ptr(), ws.numel()
     sptr = stream.cuda_stream
     adam_step = [0]
+    # NVTX ranges name each library call on the host timeline (ncu --nvtx
+    # can filter on them); they add no device work
+    nvtx = torch.cuda.nvtx
 
     def step(ev=None, tabs=None, between=None):
         """One optimizer step on `stream`: Muon, AdamW on the tail, RMNP.
         tabs: (muon, rmnp, tail) tables to use (default: the resident ones);
         between: called after the Muon call, before AdamW and RMNP."""
         m_tbl, r_tbl, t_tbl = tabs if tabs is not None else (muon_tbl, rmnp_tbl, tail_tbl)
+        nvtx.range_push("muon_owner_step")
         if ev is None:
             st = lib.muon_owner_step(m_tbl.ptr, m_tbl.n, ctypes.byref(mp), ws_ptr, ws_bytes, sptr)
         else:
             ev[0].record(stream)
             st = lib.muon_owner_step_timed(muon_tbl.ptr, muon_tbl.n, ctypes.byref(mp), ws_ptr, ws_bytes, sptr,
                                            ev[1].cuda_event, ev[2].cuda_event)
+        nvtx.range_pop()
         if st != 0:
             raise mo.MoError(st, "muon_owner_step")
         if ev is not None:
@@ -263,12 +268,16 @@ def run_ours(args, rank, world, local_rank):
         adam_step[0] += 1
         ap = mo.AdamWParams(lr=wl.adam_lr, wd=wl.adam_wd, beta1=wl.beta1, beta2=wl.beta2, eps=wl.adam_eps,
                             step=adam_step[0])
+        nvtx.range_push("adamw_tail_step")
         st = lib.adamw_tail_step(t_tbl.ptr, t_tbl.n, ctypes.byref(ap), sptr)
+        nvtx.range_pop()
         if st != 0:
             raise mo.MoError(st, "adamw_tail_step")
         if ev is not None:
             ev[4].record(stream)
+        nvtx.range_push("rmnp_step")
         st = lib.rmnp_step(r_tbl.ptr, r_tbl.n, ctypes.byref(rp), sptr)
+        nvtx.range_pop()
         if st != 0:
             raise mo.MoError(st, "rmnp_step")
         if ev is not None:
