@@ -318,8 +318,12 @@ __global__ void __launch_bounds__(256, kPrologueCtasPerSm) muon_prologue_kernel(
 // lr s / max(||V_i||, eps) for RMNP; lr s max(||V_i||, eps)^(power - 1) for
 // HTRMNP (a reading of "Optimizers In A Sharded World" section 7, which names
 // the power scaling without printing a formula).
+// max(norm, eps) that keeps a NaN norm (a NaN anywhere in the row) as NaN,
+// as F.normalize's clamp does; fmaxf would return eps for it
+__device__ __forceinline__ float clamp_norm(float nrm, float eps) { return nrm < eps ? eps : nrm; }
+
 __device__ __forceinline__ float rmnp_factor(const RmnpParams& p, float lr, float scale, float sum_sq) {
-  const float nrm = fmaxf(sqrtf(sum_sq), p.eps);
+  const float nrm = clamp_norm(sqrtf(sum_sq), p.eps);
   return p.power == 0.0f ? lr * scale / nrm : lr * scale * powf(nrm, p.power - 1.0f);
 }
 //
@@ -601,7 +605,7 @@ __global__ void __launch_bounds__(256) colcut_apply_kernel(const __grid_constant
     const int64_t r = row - p.row_prefix[ei];
     float sum = 0.f;
     for (int s = p.first[ei]; s <= p.last[ei]; ++s) sum += p.partials[p.row_prefix[s] + r];
-    const float k = p.lr * E.scale / fmaxf(sqrtf(sum), p.eps);
+    const float k = p.lr * E.scale / clamp_norm(sqrtf(sum), p.eps);
     const int C = E.C;
     const size_t off = size_t(r) * size_t(C);
     const float* __restrict__ Vr = E.V + off;

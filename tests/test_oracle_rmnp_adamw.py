@@ -45,6 +45,19 @@ def test_rmnp_zero_row_clamped():
     assert np.all(D[0] == 0) and np.array_equal(D[1], [1.0, 0, 0, 0])
 
 
+def test_rmnp_nan_row_like_library_normalize():
+    """A NaN anywhere in a row makes that whole row NaN and leaves the other
+    rows alone, as F.normalize (whose clamp keeps NaN) does."""
+    rng = np.random.default_rng(4)
+    V = rng.standard_normal((5, 9))
+    V[2, 6] = np.nan
+    ref = torch.nn.functional.normalize(torch.from_numpy(V), p=2, dim=-1).numpy()
+    D = rmnp_direction(V)
+    assert np.isnan(ref[2]).all() and np.isnan(D[2]).all()
+    keep = [0, 1, 3, 4]
+    np.testing.assert_allclose(D[keep], ref[keep], rtol=1e-14, atol=0)
+
+
 def test_rmnp_equals_polar_for_diagonal_gram():
     rng = np.random.default_rng(2)
     q, _ = np.linalg.qr(rng.standard_normal((96, 24)))
