@@ -134,7 +134,10 @@ size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_pa
  * the ns_steps iterations three grouped tcgen05 GEMM launches (Gram, A.A with
  * the b A + c A A epilogue, B.X with the a X + epilogue; with MO_NS_APPENDIX:
  * Gram, A.X, A.B with the a X + b B + epilogue); the last launch applies the
- * weight update in its epilogue. Matrices are independent. */
+ * weight update in its epilogue. Matrices are independent. Tables with a
+ * matrix of max(rows, cols) > 32768 add, after each Gram launch, one launch
+ * that sums the Gram slice partials (see mo_muon_tile_schedule); their
+ * workspace includes m x m fp32 per slice. */
 int muon_owner_step(const mo_matrix* tbl, int32_t n, const mo_muon_params* params,
                     void* ws, size_t ws_bytes, cudaStream_t stream);
 
@@ -301,7 +304,12 @@ enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
  * decreasing reduction length K (n for the Gram, m otherwise), ties broken by
  * table index, then tile row and tile column (Gram, A.A) or tile column and
  * tile row (B.X). Gram and A.A tiles cover only tiles that touch the upper
- * triangle (col_end > row_begin). */
+ * triangle (col_end > row_begin). A Gram with n > 32768 is split along its
+ * reduction into slices of 32768 columns (the last one shorter), each
+ * accumulated separately in fp32 and summed by a reduction launch: its tiles
+ * appear once per slice, with K = the slice length, after the whole
+ * matrices of equal K in (matrix, slice) order, reported with the matrix's
+ * index. */
 int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase,
                           mo_tile* out, int64_t cap, int64_t* count);
 

@@ -105,16 +105,24 @@ void free_entry(PlanEntry* e) {
 int bind_header(mo::MuonLayout& L, int32_t n, void* ws, std::vector<uint8_t>& header) {
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   header.assign(L.header_bytes, 0);
-  for (int32_t i = 0; i < n; ++i) {
-    mo::DevMat& d = L.mats[size_t(i)];
+  (void)n;
+  // the table's matrices, then the Gram slice entries of the long ones
+  for (size_t i = 0; i < L.mats.size(); ++i) {
+    mo::DevMat& d = L.mats[i];
     d.X[0] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[0]));
     d.X[1] = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.X[1]));
     d.A = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.A));
     d.B = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(d.B));
-    if (!mo::encode_matrix_maps(d, L.ns_form, header.data() + L.off_tmaps + size_t(i) * mo::kMapsPerMat * mo::kTensorMapBytes))
+    if (!mo::encode_matrix_maps(d, L.ns_form, header.data() + L.off_tmaps + i * mo::kMapsPerMat * mo::kTensorMapBytes))
       return cuda_fail(cudaErrorInvalidValue);
   }
-  std::memcpy(header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * size_t(n));
+  for (mo::GramReduce& r : L.reduces) {
+    r.A = reinterpret_cast<uint16_t*>(wsb + reinterpret_cast<uintptr_t>(r.A));
+    r.parts = reinterpret_cast<const float*>(wsb + reinterpret_cast<uintptr_t>(r.parts));
+  }
+  if (!L.reduces.empty())
+    std::memcpy(header.data() + L.off_reduces, L.reduces.data(), sizeof(mo::GramReduce) * L.reduces.size());
+  std::memcpy(header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * L.mats.size());
   std::memcpy(header.data() + L.off_seg_prefix, L.seg_prefix.data(), sizeof(int64_t) * L.seg_prefix.size());
   std::memcpy(header.data() + L.off_seg_code, L.seg_code.data(), sizeof(int32_t) * L.seg_code.size());
   for (int ph = 0; ph < 3; ++ph)
@@ -288,6 +296,13 @@ int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* pr
       const bool last = (k == 2) && (it == prm->ns_steps - 1);
       const int grid = 2 * std::max(1, std::min(np.ntiles, dev->sms / 2));
       if ((e = mo::launch_ns_phase(kinds[k], last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
+      if (k == 0 && L.reduce_blocks > 0) {
+        // long matrices: A = sum of the slice partials
+        const int rgrid = int(std::max<int64_t>(1, std::min<int64_t>(L.reduce_blocks, int64_t(dev->sms) * 4)));
+        if ((e = mo::launch_gram_reduce(reinterpret_cast<const mo::GramReduce*>(wsb + L.off_reduces),
+                                        int32_t(L.reduces.size()), L.reduce_blocks, rgrid, stream)) != cudaSuccess)
+          return cuda_fail(e);
+      }
     }
     cur ^= 1;
   }
@@ -649,7 +664,15 @@ int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase, mo_til
   int st = mo::validate_matrix_table(tbl, n);
   if (st != MO_OK) return st;
   std::vector<mo::TileRec> tiles;
-  mo::build_tiles(tbl, n, phase, mo::kBM, tiles);
+  if (phase == MO_PHASE_GRAM) {
+    // slice entries are reported with their matrix's index
+    mo::build_gram_tiles(tbl, n, mo::kBM, tiles);
+    const std::vector<mo::GramEntry> sl = mo::gram_slices(tbl, n);
+    for (mo::TileRec& t : tiles)
+      if (t.mat >= uint32_t(n)) t.mat = uint32_t(sl[t.mat - uint32_t(n)].parent);
+  } else {
+    mo::build_tiles(tbl, n, phase, mo::kBM, tiles);
+  }
   *count = int64_t(tiles.size());
   if (cap < int64_t(tiles.size())) return MO_ERR_BAD_SHAPE;
   if (!tiles.empty()) {

@@ -30,6 +30,10 @@ struct NsParams {
 // phase: MO_PHASE_GRAM, MO_PHASE_POLY, MO_PHASE_UPDATE, kPhaseAX or kPhaseABX;
 // last (UPDATE and ABX only) applies the weight update in the epilogue.
 cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, cudaStream_t stream);
+// A = bf16(sum of the slice partials) for the long matrices, upper part and
+// mirror; `blocks` 64 x 64 upper blocks over the `count` records.
+cudaError_t launch_gram_reduce(const GramReduce* reduces, int32_t count, int64_t blocks, int grid,
+                               cudaStream_t stream);
 // Writes kMapsPerMat CUtensorMap; with MO_NS_APPENDIX the B buffer is m x n.
 bool encode_matrix_maps(const DevMat& d, int ns_form, void* out_maps);
 cudaError_t device_status_ptr(int** out);

@@ -28,6 +28,13 @@ constexpr int kCastTC = 128;
 constexpr int64_t kMaxDim = int64_t(1) << 22;   // rows or cols
 constexpr int64_t kMaxM = 65536;                 // min(rows, cols)
 
+// Gram products longer than this along their reduction (n) are split into
+// slices of this many columns: each slice accumulates its own fp32 partial
+// (tcgen05 accumulation over very long reductions drops products far below
+// the running sum: measured on a 1 x 2^20 matrix, a 4% error), and a
+// reduction launch sums the partials in a fixed order.
+constexpr int64_t kGramSliceK = 32768;
+
 // Number of CUtensorMap objects per matrix: X ping, X pong, A, B.
 constexpr int kMapsPerMat = 4;
 constexpr size_t kTensorMapBytes = 128;
@@ -50,6 +57,18 @@ struct DevMat {
   float rms_scale;          // 0.2 sqrt(max(R, C)) (match_rms_adamw)
   int64_t nrm_base;         // first sum-of-squares chunk (global index)
   int64_t nrm_count;        // sum-of-squares chunks of this matrix
+  int32_t gram_partial;     // a Gram slice entry: n is the slice length, X points at its first
+                            // column, A is its fp32 [m, lda] partial (upper tiles, no mirror)
+  int32_t pad0;
+};
+
+// One long matrix whose Gram is summed from slice partials.
+struct GramReduce {
+  uint16_t* A;              // [m, lda] bf16 result (upper part and mirror)
+  const float* parts;       // `slices` fp32 [m, lda] partials, part_stride floats apart
+  int64_t part_stride;
+  int64_t block_base;       // first 64 x 64 upper block of this matrix in the launch
+  int32_t m, lda, slices, pad;
 };
 
 // Newton-Schulz launch kinds beyond the public MO_PHASE_* values: the two

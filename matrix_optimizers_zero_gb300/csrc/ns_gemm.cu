@@ -151,6 +151,24 @@ __device__ __forceinline__ void epilogue_symmetric(const NsParams& p, const DevM
     float v[32];
     tmem_chunk(tb + uint32_t(ch * 32), v);
     if (!rv || col0 >= m) continue;
+    if (PHASE == MO_PHASE_GRAM && M.gram_partial) {
+      // a slice of a long Gram: the fp32 tile as is (no rounding, no mirror)
+      float* o = reinterpret_cast<float*>(M.A) + size_t(row) * ld + col0;
+      if (col0 + 32 <= m) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w8[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w8[j] = __float_as_uint(v[8 * q + j]);
+          ptx::st_global_v8(o + 8 * q, w8);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < m) o[i] = v[i];
+      }
+      continue;
+    }
     if (PHASE == MO_PHASE_POLY) {
       float a[32];
       chunk_operand(a_row, col0, m, pre, a);
@@ -513,6 +531,77 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
+// A = bf16(sum over slices of the fp32 partials) for each long matrix: one
+// 64 x 64 upper block (column block >= row block) per iteration, partials
+// summed in slice order, the upper part stored directly and the strict lower
+// part through a shared-memory transpose, so every element of A is written
+// once.
+__global__ void __launch_bounds__(256) gram_reduce_kernel(const GramReduce* __restrict__ recs, int32_t count,
+                                                          int64_t blocks) {
+  __shared__ float tile[64][65];
+  const int tid = int(threadIdx.x), tx = tid & 15, ty = tid >> 4;
+  for (int64_t b = blockIdx.x; b < blocks; b += gridDim.x) {
+    int lo = 0, hi = count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (recs[mid].block_base <= b) lo = mid; else hi = mid - 1;
+    }
+    const GramReduce R = recs[lo];
+    const int64_t local = b - R.block_base;
+    // upper blocks are numbered row by row; row br starts at br nb - br (br - 1) / 2
+    const int nb = (R.m + 63) / 64;
+    int br = 0, hb = nb - 1;
+    while (br < hb) {
+      const int mid = (br + hb + 1) >> 1;
+      if (int64_t(mid) * nb - int64_t(mid) * (mid - 1) / 2 <= local) br = mid; else hb = mid - 1;
+    }
+    const int bc = br + int(local - (int64_t(br) * nb - int64_t(br) * (br - 1) / 2));
+    const int r0 = br * 64, c0 = bc * 64 + tx * 4;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    for (int sl = 0; sl < R.slices; ++sl) {
+      const float* P = R.parts + int64_t(sl) * R.part_stride;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = r0 + ty * 4 + i;
+        if (r < R.m) {
+          const float4 x = *reinterpret_cast<const float4*>(P + size_t(r) * size_t(R.lda) + c0);
+          acc[i][0] += x.x;
+          acc[i][1] += x.y;
+          acc[i][2] += x.z;
+          acc[i][3] += x.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = r0 + ty * 4 + i;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        tile[ty * 4 + i][tx * 4 + j] = acc[i][j];
+        const int c = c0 + j;
+        if (r < R.m && c < R.m && c >= r) R.A[size_t(r) * size_t(R.lda) + c] = float_to_bf16_bits(acc[i][j]);
+      }
+    }
+    __syncthreads();
+    // mirror: A[c][r] = value at (r, c) for c > r
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = bc * 64 + ty * 4 + i;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = r0 + tx * 4 + j;
+        if (c < R.m && r < R.m && c > r)
+          R.A[size_t(c) * size_t(R.lda) + r] = float_to_bf16_bits(tile[tx * 4 + j][ty * 4 + i]);
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // Single-CTA kernel that waits on a barrier nothing completes; exercises the
 // bounded-wait path.
 __global__ void bounded_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
@@ -573,6 +662,13 @@ cudaError_t launch_ns_phase(int phase, bool last, const NsParams& p, int grid, c
       return last ? launch_pair<MO_PHASE_UPDATE, true>(p, grid, stream)
                   : launch_pair<MO_PHASE_UPDATE, false>(p, grid, stream);
   }
+}
+
+cudaError_t launch_gram_reduce(const GramReduce* reduces, int32_t count, int64_t blocks, int grid,
+                               cudaStream_t stream) {
+  if (count <= 0 || blocks <= 0) return cudaSuccess;
+  gram_reduce_kernel<<<grid, 256, 0, stream>>>(reduces, count, blocks);
+  return cudaGetLastError();
 }
 
 cudaError_t device_status_ptr(int** out) {

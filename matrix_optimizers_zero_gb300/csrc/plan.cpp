@@ -157,6 +157,49 @@ void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector
   for (size_t j = 0; j < keys.size(); ++j) out[j] = keys[j].t;
 }
 
+std::vector<GramEntry> gram_slices(const mo_matrix* tbl, int32_t n) {
+  std::vector<GramEntry> out;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t nn = std::max(tbl[i].rows, tbl[i].cols);
+    if (nn <= kGramSliceK) continue;
+    for (int64_t k0 = 0, s = 0; k0 < nn; k0 += kGramSliceK, ++s)
+      out.push_back({i, int32_t(s), k0, std::min(kGramSliceK, nn - k0)});
+  }
+  return out;
+}
+
+void build_gram_tiles(const mo_matrix* tbl, int32_t n, int bm, std::vector<TileRec>& out) {
+  struct Key {
+    int64_t k;
+    TileRec t;
+  };
+  std::vector<Key> keys;
+  auto add = [&](int64_t m, int64_t k, uint32_t idx) {
+    const int64_t tiles_m = ceil_div(m, bm), tiles_n = ceil_div(m, kBN);
+    for (int64_t tm = 0; tm < tiles_m; ++tm)
+      for (int64_t tn = 0; tn < tiles_n; ++tn)
+        if ((tn + 1) * kBN > tm * bm) keys.push_back({k, {idx, uint16_t(tm), uint16_t(tn)}});
+  };
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t m = std::min(tbl[i].rows, tbl[i].cols), nn = std::max(tbl[i].rows, tbl[i].cols);
+    if (nn <= kGramSliceK) add(m, nn, uint32_t(i));
+  }
+  const std::vector<GramEntry> sl = gram_slices(tbl, n);
+  for (size_t j = 0; j < sl.size(); ++j) {
+    const mo_matrix& t = tbl[sl[j].parent];
+    add(std::min(t.rows, t.cols), sl[j].k, uint32_t(n) + uint32_t(j));
+  }
+  // longest reduction first, then entry, tile row, tile column
+  std::sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
+    if (a.k != b.k) return a.k > b.k;
+    if (a.t.mat != b.t.mat) return a.t.mat < b.t.mat;
+    if (a.t.tm != b.t.tm) return a.t.tm < b.t.tm;
+    return a.t.tn < b.t.tn;
+  });
+  out.resize(keys.size());
+  for (size_t j = 0; j < keys.size(); ++j) out[j] = keys[j].t;
+}
+
 void order_prologue(MuonLayout& L, int64_t window) {
   // Norm segments in table order; the cast segment of matrix i follows once
   // `window` items (about one wave of the launch) have been listed after the
@@ -220,13 +263,26 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout&
   L.nrm_items = chunks;
   L.cast_items = casts;
   order_prologue(L, int64_t(kPrologueCtasPerSm) * 152);
-  for (int ph = 0; ph < 3; ++ph) build_tiles(tbl, n, ph, bm, L.tiles[ph]);
+  build_gram_tiles(tbl, n, bm, L.tiles[MO_PHASE_GRAM]);
+  build_tiles(tbl, n, MO_PHASE_POLY, bm, L.tiles[MO_PHASE_POLY]);
+  build_tiles(tbl, n, MO_PHASE_UPDATE, bm, L.tiles[MO_PHASE_UPDATE]);
+  // Gram slice entries of the long matrices (buffers assigned below)
+  const std::vector<GramEntry> slices = gram_slices(tbl, n);
+  for (const GramEntry& e : slices) {
+    DevMat d = L.mats[size_t(e.parent)];
+    d.n = int32_t(e.k);
+    d.gram_partial = 1;
+    L.mats.push_back(d);
+  }
+  const size_t nall = L.mats.size();
+  L.reduces.clear();
+  L.reduce_blocks = 0;
 
   size_t off = 0;
   L.off_meta = off;
-  off = align_up(off + sizeof(DevMat) * size_t(n), 128);
+  off = align_up(off + sizeof(DevMat) * nall, 128);
   L.off_tmaps = off;
-  off = align_up(off + kTensorMapBytes * kMapsPerMat * size_t(n), 256);
+  off = align_up(off + kTensorMapBytes * kMapsPerMat * nall, 256);
   L.off_seg_prefix = off;
   off = align_up(off + sizeof(int64_t) * L.seg_prefix.size(), 256);
   L.off_seg_code = off;
@@ -239,6 +295,24 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout&
   off = align_up(off + sizeof(uint32_t), 256);
   L.off_lr = off;
   off = align_up(off + sizeof(float), 256);
+  {
+    // one reduction record per long matrix
+    int32_t prev = -1;
+    for (const GramEntry& e : slices)
+      if (e.parent != prev) {
+        prev = e.parent;
+        GramReduce r{};
+        r.m = L.mats[size_t(e.parent)].m;
+        r.lda = L.mats[size_t(e.parent)].lda;
+        r.slices = int32_t(ceil_div(std::max(tbl[e.parent].rows, tbl[e.parent].cols), kGramSliceK));
+        r.block_base = L.reduce_blocks;
+        const int64_t nb = ceil_div(r.m, 64);
+        L.reduce_blocks += nb * (nb + 1) / 2;
+        L.reduces.push_back(r);
+      }
+  }
+  L.off_reduces = off;
+  off = align_up(off + sizeof(GramReduce) * L.reduces.size(), 256);
   for (int ph = 0; ph < 3; ++ph) {
     L.off_tiles[ph] = off;
     off = align_up(off + sizeof(TileRec) * L.tiles[ph].size(), 256);
@@ -263,6 +337,26 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout&
     off = align_up(off + ab, 1024);
     d.B = reinterpret_cast<uint16_t*>(off);
     off = align_up(off + bb, 1024);
+  }
+  // slice entries: X at the slice's first column of the matrix's iterates,
+  // A at the slice's fp32 partial (S consecutive partials per long matrix)
+  size_t r = 0;
+  for (size_t j = 0; j < slices.size(); ++j) {
+    const GramEntry& e = slices[j];
+    const DevMat& par = L.mats[size_t(e.parent)];
+    DevMat& d = L.mats[size_t(n) + j];
+    d.X[0] = reinterpret_cast<uint16_t*>(reinterpret_cast<uintptr_t>(par.X[0]) + size_t(e.k0) * 2);
+    d.X[1] = reinterpret_cast<uint16_t*>(reinterpret_cast<uintptr_t>(par.X[1]) + size_t(e.k0) * 2);
+    d.B = par.B;
+    const size_t pb = size_t(par.m) * size_t(par.lda) * 4;
+    if (e.slice == 0) {   // the reduction records follow the long matrices in table order
+      L.reduces[r].A = par.A;
+      L.reduces[r].parts = reinterpret_cast<const float*>(off);
+      L.reduces[r].part_stride = int64_t(align_up(pb, 1024) / 4);
+      ++r;
+    }
+    d.A = reinterpret_cast<uint16_t*>(off);
+    off = align_up(off + pb, 1024);
   }
   L.total_bytes = off;
 }

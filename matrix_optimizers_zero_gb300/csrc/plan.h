@@ -12,7 +12,7 @@
 namespace mo {
 
 struct MuonLayout {
-  int32_t n = 0;
+  int32_t n = 0;                     // matrices of the table; mats[n..] are Gram slice entries
   int32_t ns_form = MO_NS_GRAM;
   std::vector<DevMat> mats;          // buffer pointers hold workspace OFFSETS until bound
   // Prologue work list: 2n segments, the momentum/norm chunks of every
@@ -23,12 +23,15 @@ struct MuonLayout {
   std::vector<int64_t> seg_prefix;   // 2n + 1 prefix sums of segment sizes
   std::vector<int32_t> seg_code;     // 2n codes: matrix * 2 + (0 = norm chunks, 1 = cast tiles)
   std::vector<int64_t> nrm_items, cast_items;   // per matrix
-  std::vector<TileRec> tiles[3];     // per phase, launch order
+  std::vector<TileRec> tiles[3];     // per phase, launch order (Gram tiles may name slice entries)
+  std::vector<GramReduce> reduces;   // long matrices (pointer fields hold offsets until bound)
+  int64_t reduce_blocks = 0;         // 64 x 64 upper blocks over all long matrices
   int64_t nrm_total = 0;
   int64_t cast_total = 0;
   size_t off_meta = 0, off_tmaps = 0, off_seg_prefix = 0, off_seg_code = 0, off_counters = 0, off_ready = 0,
          off_abort = 0;
-  size_t off_lr = 0;                 // one fp32: the learning rate a planned step reads (mo_muon_plan)
+  size_t off_lr = 0;
+  size_t off_reduces = 0;                 // one fp32: the learning rate a planned step reads (mo_muon_plan)
   size_t off_tiles[3] = {0, 0, 0};
   size_t header_bytes = 0;           // [0, header_bytes) is uploaded by every call
   size_t off_partials = 0, off_scales = 0, off_buffers = 0;
@@ -46,6 +49,19 @@ int validate_adamw(const mo_tail_seg* segs, int32_t n, const mo_adamw_params* p)
 // Tile schedule of one phase (MO_PHASE_*), sorted into launch order; bm is
 // the output tile height (128 rows for one CTA, 256 for a CTA pair).
 void build_tiles(const mo_matrix* tbl, int32_t n, int phase, int bm, std::vector<TileRec>& out);
+
+// Gram work entries: the matrices with n <= kGramSliceK, and one slice entry
+// per kGramSliceK columns of the longer ones. Entry e < n is matrix e; slice
+// entries follow in (matrix, slice) order.
+struct GramEntry {
+  int32_t parent;
+  int32_t slice;     // -1 for a whole matrix
+  int64_t k0, k;     // first column and length along the reduction
+};
+std::vector<GramEntry> gram_slices(const mo_matrix* tbl, int32_t n);
+
+// Gram tile schedule over the entries above (TileRec::mat = entry index).
+void build_gram_tiles(const mo_matrix* tbl, int32_t n, int bm, std::vector<TileRec>& out);
 
 // (Re)orders the prologue work list for a launch that processes about
 // `window` items at a time (CTAs in flight); plan_muon uses 4 x 152.

@@ -49,6 +49,7 @@ def test_status_strings(lib):
 # ---------------------------------------------------------------- schedules
 
 BM = 256   # output tile height of the CTA-pair kernel
+GRAM_SLICE = 32768   # Gram reductions longer than this are split into slices of this length
 
 
 def py_schedule(shapes, phase):
@@ -61,22 +62,42 @@ def py_schedule(shapes, phase):
             for tm in range(tiles_m):
                 for tn in range(-(-n // 256)):
                     keys.append((-m, i, tn, tm))
-        else:
+        elif phase == mo.PHASE_POLY or n <= GRAM_SLICE:
             k = n if phase == mo.PHASE_GRAM else m
             for tm in range(tiles_m):
                 for tn in range(-(-m // 256)):
                     if (tn + 1) * 256 > tm * BM:
-                        keys.append((-k, i, tm, tn))
+                        keys.append((-k, i, tm, tn, i))
+    if phase == mo.PHASE_GRAM:
+        # longer Grams: one entry per GRAM_SLICE columns, numbered after the
+        # table's matrices in (matrix, slice) order, reported as the matrix
+        entry = len(shapes)
+        for i, (R, C) in enumerate(shapes):
+            m, n = min(R, C), max(R, C)
+            if n <= GRAM_SLICE:
+                continue
+            for k0 in range(0, n, GRAM_SLICE):
+                k = min(GRAM_SLICE, n - k0)
+                for tm in range(-(-m // BM)):
+                    for tn in range(-(-m // 256)):
+                        if (tn + 1) * 256 > tm * BM:
+                            keys.append((-k, entry, tm, tn, i))
+                entry += 1
     keys.sort()
     if phase == mo.PHASE_UPDATE:
         return [(i, tm, tn) for _, i, tn, tm in keys]
-    return [(i, tm, tn) for _, i, tm, tn in keys]
+    return [(i, tm, tn) for _, _, tm, tn, i in keys]
+
+
+def gram_slices(n):
+    return max(1, -(-n // GRAM_SLICE)) if n > GRAM_SLICE else 1
 
 
 TABLES = {
     "gpt2l": [(s.rows, s.cols) for s in workloads.get_workload("gpt2l").matrices],
     "share32b": [(s.rows, s.cols) for s in workloads.get_workload("share32b").matrices],
     "ragged": [(130, 257), (257, 130), (1, 9), (9, 1), (128, 256), (300, 300), (1000, 70)],
+    "long": [(3, 100_000), (70_000, 300), (130, 257), (600, 32_768), (32_769, 5), (1, 1 << 22)],
 }
 
 
@@ -87,8 +108,10 @@ def test_schedule_bit_exact(lib, table, phase):
     assert mo.mo_muon_tile_schedule(shapes, phase) == py_schedule(shapes, phase)
 
 
-@pytest.mark.parametrize("shape", [(130, 257), (257, 130), (300, 300), (700, 1500), (1, 5)])
+@pytest.mark.parametrize("shape", [(130, 257), (257, 130), (300, 300), (700, 1500), (1, 5), (300, 70_000)])
 def test_schedule_covers_outputs_exactly_once(lib, shape):
+    """Once per Gram slice for the Gram (whose slices each cover the whole
+    output), once otherwise."""
     m, n = min(shape), max(shape)
     for phase in (0, 1):
         cover = np.zeros((m, m), dtype=np.int32)
@@ -101,7 +124,7 @@ def test_schedule_covers_outputs_exactly_once(lib, shape):
                         cover[r, c] += 1
                     if c > r:
                         cover[c, r] += 1
-        assert np.all(cover == 1), phase
+        assert np.all(cover == (gram_slices(n) if phase == 0 else 1)), phase
     cover = np.zeros((m, n), dtype=np.int32)
     for _, tm, tn in mo.mo_muon_tile_schedule([shape], 2):
         cover[tm * BM:tm * BM + BM, tn * 256:tn * 256 + 256] += 1
