@@ -49,10 +49,13 @@ def test_gram_split_into_slices(form):
     wl = workloads.custom_workload(shapes, w_std=0.0, g_std=1e-3)
     host = [workloads.host_matrix(wl, i, v_std=1e-3) for i in range(len(shapes))]
     p = mo.MuonParams(ns_form=form)
-    dev = to_device(host, DEV)
-    mo.muon_owner_step(dev, p, mo.muon_workspace(dev, p, device=DEV))
+    dev, again = to_device(host, DEV), to_device(host, DEV)
+    for mats in (dev, again):
+        mo.muon_owner_step(mats, p, mo.muon_workspace(mats, p, device=DEV))
     torch.cuda.synchronize()
     assert mo.mo_last_device_error() == 0
+    for (Wa, _, Va), (Wb, _, Vb) in zip(dev, again):   # partials are summed in a fixed order
+        assert torch.equal(Wa, Wb) and torch.equal(Va, Vb)
     tol = 2e-2 if form == "appendix" else NS_REL_FROB_TOL
     for (Wh, Gh, Vh), (Wd, _, Vd) in zip(host, dev):
         R, C = Wh.shape
