@@ -416,6 +416,20 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     e2e_ms_max = max_over_ranks(e0.elapsed_time(e1) / max(e2e_steps, 1), dev)
     e2e_value = whole_job_tflops(world, ns_flops, e2e_ms_max)
+    # the host link as this run sees it: one plain pinned copy each way, so a
+    # link-bound e2e figure can be read against what the link delivered
+    link = None
+    if pin:
+        l0, l1, l2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        with torch.cuda.stream(s_out):
+            l0.record(s_out)
+            hW.copy_(Wf, non_blocking=True)
+            l1.record(s_out)
+            Gf.copy_(hG, non_blocking=True)
+            l2.record(s_out)
+        l2.synchronize()
+        link = {"d2h_gbs": round(hW.numel() * 4 / (l0.elapsed_time(l1) * 1e-3) / 1e9, 1),
+                "h2d_gbs": round(hG.numel() * 2 / (l1.elapsed_time(l2) * 1e-3) / 1e9, 1)}
     if mo.mo_last_device_error() != 0:
         raise RuntimeError("device-side timeout during the timed region")
 
@@ -484,6 +498,7 @@ def run_ours(args, rank, world, local_rank):
         },
         "e2e": ({"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                  "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms_max, 3), "steps": e2e_steps,
+                 "link_measured": link,
                  "copies": "pinned host buffers; uploads, compute and read-backs on three streams, "
                            "gradients double-buffered on the device"}
                 if e2e_steps else None),
