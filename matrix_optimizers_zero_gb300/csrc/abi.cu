@@ -102,10 +102,9 @@ void free_entry(PlanEntry* e) {
 }
 
 // Binds a planned layout to `ws` and builds its header image.
-int bind_header(mo::MuonLayout& L, int32_t n, void* ws, std::vector<uint8_t>& header) {
+int bind_header(mo::MuonLayout& L, void* ws, std::vector<uint8_t>& header) {
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   header.assign(L.header_bytes, 0);
-  (void)n;
   // the table's matrices, then the Gram slice entries of the long ones
   for (size_t i = 0; i < L.mats.size(); ++i) {
     mo::DevMat& d = L.mats[i];
@@ -132,7 +131,7 @@ int bind_header(mo::MuonLayout& L, int32_t n, void* ws, std::vector<uint8_t>& he
 }
 
 int build_entry(PlanEntry& E, const mo_matrix* tbl, int32_t n, void* ws) {
-  const int st = bind_header(E.L, n, ws, E.header);
+  const int st = bind_header(E.L, ws, E.header);
   if (st != MO_OK) return st;
   E.table.assign(tbl, tbl + n);
   E.ws = reinterpret_cast<uintptr_t>(ws);
@@ -451,7 +450,7 @@ int mo_muon_plan_create(const mo_matrix* tbl, int32_t n, const mo_muon_params* p
   }
   mo::order_prologue(P->L, int64_t(mo::kPrologueCtasPerSm) * dev->sms);
   std::vector<uint8_t> header;
-  if ((st = bind_header(P->L, n, ws, header)) != MO_OK) {
+  if ((st = bind_header(P->L, ws, header)) != MO_OK) {
     delete P;
     return st;
   }

@@ -155,6 +155,27 @@ def test_workspace_bytes(lib):
                                        ctypes.byref(mo.MuonParams(nesterov=True, lr_adjust="match_rms_adamw"))) == nb2
 
 
+def test_workspace_bytes_with_gram_slices(lib):
+    """A matrix with n > 32768 adds one fp32 m x m partial (rows padded to 64
+    elements) per Gram slice; shorter ones add nothing."""
+    p = mo.MuonParams()
+
+    def ws(shapes):
+        arr = mo.fake_table(shapes)
+        return lib.mo_muon_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), len(shapes), ctypes.byref(p))
+
+    for (R, C), slices in (((300, 70_000), 3), ((40_000, 130), 2), ((1, 1 << 20), 32)):
+        m = min(R, C)
+        lda = -(-m // 64) * 64
+        part = -(-(m * lda * 4) // 1024) * 1024
+        base = ws([(R, C), (130, 257)])
+        # the same matrix just under the threshold has no slices
+        short = ws([(min(R, C), 32_768) if R < C else (32_768, min(R, C)), (130, 257)])
+        x_extra = 2 * m * (-(-max(R, C) // 64) * 64 - 32_768) * 2
+        assert base - short >= slices * part + x_extra - 4096
+        assert base - short <= slices * part + x_extra + 64 * 1024
+
+
 # ---------------------------------------------------------------- validation (no GPU needed)
 
 def _muon(lib, arr, n, params, ws=1 << 30, ws_bytes=1 << 40):
