@@ -517,8 +517,9 @@ def run_ours(args, rank, world, local_rank):
 
 def measure_extras(args, mo, workloads, wl, shapes, W_l, G_l, V_l, Wr_l, Vr_l, dev, stream, peaks):
     """Times the kernels beyond the benchmarked step on the same table (not
-    part of the headline step): the Muon variants, column-cut RMNP, HTRMNP and
-    the host-side owner planner. CUDA events on `stream`, 2 warm-up + 5 timed
+    part of the headline step): the Muon variants, column-cut RMNP, HTRMNP,
+    the planned Muon step replayed from a CUDA graph, and the host-side owner
+    planner. CUDA events on `stream`, 2 warm-up + 5 timed
     calls each."""
     import time
     import torch
@@ -603,6 +604,32 @@ def measure_extras(args, mo, workloads, wl, shapes, W_l, G_l, V_l, Wr_l, Vr_l, d
     gbs = n_el * 22 / (ms * 1e-3) / 1e9
     out["rmnp_colcut_4_shards"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
                                    "bytes_per_el": 22}
+
+    # the planned Muon step replayed from a CUDA graph against per-call
+    # steps, on the whole table and on its first four matrices (one layer),
+    # where launch and host overhead weigh most
+    def graph_vs_eager(name, sub):
+        t = mo.MuonTable(sub)
+        p = mo.MuonParams(lr=wl.lr, wd=wl.wd, mu=wl.mu)
+        ws_e = mo.muon_workspace(t, p, device=dev)
+        eager = timed(lambda: mo.muon_owner_step(t, p, ws_e, stream=stream))
+        plan = mo.MuonPlan(t, p, stream=stream)
+        plan.step(stream=stream)                 # first launches outside the capture
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            plan.step()
+
+        def replay():
+            with torch.cuda.stream(stream):
+                graph.replay()
+
+        replayed = timed(replay)
+        plan.close()
+        out[name] = {"matrices": len(sub), "per_call_ms": round(eager, 4), "graph_replay_ms": round(replayed, 4)}
+
+    graph_vs_eager("muon_graph_replay_table", mats)
+    graph_vs_eager("muon_graph_replay_one_layer", mats[:4])
 
     # owner planner (host only): GPT-2 Large-style roles over 8 ranks
     roles = workloads.owner_roles(wl, 4 if len(shapes) % 4 == 0 else 1)
