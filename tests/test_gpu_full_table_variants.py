@@ -85,3 +85,38 @@ def test_htrmnp_full_table_sampled_rows():
         Wn = oracle.decoupled_update(W0, oracle.htrmnp_direction(Vn), p.lr, p.wd, oracle.shape_scale(R, C))
         assert max_rel(f64(dev[i][2][rows]), Vn) <= FP32_MAX_REL_TOL
         assert max_rel(f64(dev[i][0][rows]), Wn) <= FP32_MAX_REL_TOL
+
+
+def test_colcut_rmnp_full_table_equals_unsharded():
+    """Every matrix cut into 4 column shards (own buffers; at most 512 shards,
+    whole matrices, per call, as the benchmark's extras run it): each
+    reassembled matrix equals the unsharded RMNP step (with the column-cut
+    form's clamp, 1e-7) within fp32 reassociation."""
+    wl = workloads.get_workload("gpt2l")
+    dev = workloads.device_matrices(wl, DEV, v_std=1e-3)
+    p = mo.RmnpParams(lr=wl.lr, wd=wl.wd, mu=wl.mu, eps=1e-7)
+    shards, groups, scales, cuts = [], [], [], []
+    for g_id, (W, G, V) in enumerate(dev):
+        R, C = W.shape
+        edges = [C * k // 4 for k in range(5)]
+        cuts.append(edges)
+        for a, b in zip(edges[:-1], edges[1:]):
+            shards.append((W[:, a:b].contiguous(), G[:, a:b].contiguous(), V[:, a:b].contiguous()))
+            groups.append(g_id)
+            scales.append(oracle.shape_scale(R, C))
+    k = 0
+    while k < len(shards):
+        j = min(len(shards), k + 512)
+        while j < len(shards) and groups[j] == groups[j - 1]:
+            j -= 1
+        mo.rmnp_colcut_step(shards[k:j], groups[k:j], scales[k:j], p)
+        k = j
+    mo.rmnp_step(dev, p)
+    torch.cuda.synchronize()
+    for g_id in SAMPLE:
+        W, _, V = dev[g_id]
+        mine = [s for s, g in zip(shards, groups) if g == g_id]
+        Wc = torch.cat([s[0] for s in mine], dim=1)
+        Vc = torch.cat([s[2] for s in mine], dim=1)
+        assert max_rel(f64(Vc), f64(V)) <= FP32_MAX_REL_TOL
+        assert max_rel(f64(Wc), f64(W)) <= FP32_MAX_REL_TOL
