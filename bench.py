@@ -4,9 +4,12 @@ One step = the whole hot path over one owner's table: the Muon step on every
 2D matrix (momentum, Frobenius normalisation, five quintic Newton-Schulz
 iterations, shape-scaled update with weight decay), AdamW on the packed
 non-matrix tail, and RMNP on the same matrices (its own momentum and weight
-copies). Default workload: the GPT-2 Large matrix set (144 matrices, 707.8 M
-elements; tail 601,600 elements), synthetic seeded inputs resident in HBM.
-The working set (~17 GB) is far larger than L2, so no flush is needed.
+copies). Default workload: the Llama-style 8B matrix set (224 matrices,
+6.98 G elements; AdamW tail 1.05 G elements: the RMSNorm vectors, the
+embedding and the LM head), synthetic seeded inputs resident in HBM. The
+working set (~200 GB) is far larger than L2, so no flush is needed. After the
+headline the GPT-2 Large matrix set (144 matrices) is timed the same way and
+reported under `secondary` (device-resident inputs only).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
 
@@ -31,14 +34,20 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "owner Muon step ms & NS TFLOP/s vs bf16 peak; RMNP/AdamW HBM GB/s"
-
-# DRAM bytes of one step's 15 Newton-Schulz launches on the GPT-2 Large table,
-# from ncu (dram__bytes_read.sum + dram__bytes_write.sum, one pass) over the 15
-# NS launches of one step on the full table
-# (profiles/ns_gemm_pair_gpt2l_tensor_active.md).
-# Valid only for the kernel source and tile schedule it was measured on.
-NS_TRAFFIC = {"source_sha256_16": "27380c248ef7ee14", "workload": "gpt2l", "bytes_per_ns_segment": 36.92e9}
+DEFAULT_CONFIG = "llama8b"
+SECONDARY_CONFIG = "gpt2l"
 UNIT = "TFLOP/s"
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one step's 15
+# Newton-Schulz launches, per workload, from an ncu capture of the named
+# capture workload scaled by `scale` (the capture workload holds 1/scale of
+# the table's matrices). Valid only for the kernel source and tile schedule it
+# was measured on (hash of ns_gemm.cu and plan.cpp); the profiles directory
+# holds the capture summaries with their commands.
+NS_TRAFFIC = {}
+# A timed region at least this long is "a kernel timed inside a long step":
+# its roofline uses the sustained bf16 peak, a shorter one the burst peak.
+SUSTAINED_REGION_S = 1.0
 
 
 def load_peaks():
@@ -52,18 +61,33 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def ns_traffic(workload: str):
-    """The profiled DRAM traffic of the NS launches, or None when the kernel
-    or its tile schedule differs from the one profiled (or for another
-    workload)."""
+def choose_peak(peaks, region_s: float):
+    """(peak TFLOP/s, name): the sustained bf16 peak for a timed region of at
+    least SUSTAINED_REGION_S seconds, the burst peak for a shorter one."""
+    if region_s >= SUSTAINED_REGION_S:
+        return peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
+    return peaks["bf16_tflops"], "bf16_tflops (burst)"
+
+
+def source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     for name in ("ns_gemm.cu", "plan.cpp"):
         with open(os.path.join(ROOT, "matrix_optimizers_zero_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
-    if h.hexdigest()[:16] != NS_TRAFFIC["source_sha256_16"] or workload != NS_TRAFFIC["workload"]:
-        return None
-    return NS_TRAFFIC["bytes_per_ns_segment"]
+    return h.hexdigest()[:16]
+
+
+def ns_traffic(workload: str):
+    """(bytes, note): the profiled DRAM traffic of one step's NS launches for
+    this workload, or (None, why) when there is no capture for it or the
+    kernel or its tile schedule differs from the one profiled."""
+    rec = NS_TRAFFIC.get(workload)
+    if rec is None:
+        return None, "no capture for this workload"
+    if rec["source_sha256_16"] != source_hash():
+        return None, "kernel source changed since the capture"
+    return rec["bytes_per_ns_segment"], rec["how"]
 
 
 # ---------------------------------------------------------------- multi-rank helpers
@@ -149,114 +173,159 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def cpu_oracle_sample(wl, max_seconds=20.0, indices=None, min_seconds=0.0):
-    """Times the CPU oracle (as it stands) on a bounded sample of the
-    workload: whole-matrix Muon steps on one matrix per distinct shape, in
-    table order (repeated until min_seconds of work), stopping once
-    max_seconds is spent. Returns (TFLOP/s, seconds, description, cores)."""
-    import numpy as np
-    import oracle
+def distinct_shapes_by_cost(wl):
+    """Index of the first matrix of each distinct shape, cheapest NS first."""
     from matrix_optimizers_zero_gb300 import workloads
-    cores = len(os.sched_getaffinity(0))
     seen, picks = set(), []
     for i, s in enumerate(wl.matrices):
         if (s.rows, s.cols) not in seen:
             seen.add((s.rows, s.cols))
             picks.append(i)
-    if indices is not None:
-        picks = indices
+    return sorted(picks, key=lambda i: (workloads.ns_alg_flops(wl.matrices[i].rows, wl.matrices[i].cols,
+                                                               wl.ns_steps), i))
+
+
+def oracle_matrix_seconds(wl, i):
+    """Seconds the oracle's whole-matrix Muon step takes on matrix i (seeded
+    host inputs, momentum from an earlier step), and that step's NS flops."""
+    import oracle
+    from matrix_optimizers_zero_gb300 import workloads
+    W, G, V = workloads.host_matrix(wl, i, v_std=1e-3)
+    W, G, V = (t.float().double().numpy() for t in (W, G, V))
+    t0 = time.perf_counter()
+    oracle.muon_matrix_step(W, G, V, lr=wl.lr, wd=wl.wd, mu=wl.mu, ns_steps=wl.ns_steps)
+    s = wl.matrices[i]
+    return time.perf_counter() - t0, workloads.ns_alg_flops(s.rows, s.cols, wl.ns_steps)
+
+
+def cpu_oracle_sample(wl, max_seconds=25.0, min_seconds=10.0):
+    """Times the CPU oracle (as it stands) on a bounded sample of the
+    workload: whole-matrix Muon steps on one matrix per distinct shape,
+    cheapest first, skipping a shape whose predicted time would overrun
+    max_seconds, and cycling again while less than min_seconds were spent.
+    The full table's oracle step time is extrapolated from the measured rate.
+    Returns a dict (TFLOP/s, seconds, description, cores, extrapolated step
+    seconds)."""
+    from matrix_optimizers_zero_gb300 import workloads
+    cores = len(os.sched_getaffinity(0))
+    picks = distinct_shapes_by_cost(wl)
     flops = 0
     t_total = 0.0
     done = []
-    order = list(picks) * (8 if min_seconds > 0 else 1)
-    for k, i in enumerate(order):
-        if k >= len(picks) and t_total >= min_seconds:
+    for rnd in range(8):
+        ran = False
+        for i in picks:
+            s = wl.matrices[i]
+            f = workloads.ns_alg_flops(s.rows, s.cols, wl.ns_steps)
+            if done and t_total + f / (flops / t_total) > max_seconds:
+                continue
+            secs, f = oracle_matrix_seconds(wl, i)
+            t_total += secs
+            flops += f
+            done.append(f"{s.rows}x{s.cols}")
+            ran = True
+        if t_total >= min_seconds or not ran:
             break
-        W, G, V = workloads.host_matrix(wl, i, v_std=1e-3)
-        W, G, V = (t.float().double().numpy() for t in (W, G, V))
-        t0 = time.perf_counter()
-        oracle.muon_matrix_step(W, G, V, lr=wl.lr, wd=wl.wd, mu=wl.mu, ns_steps=wl.ns_steps)
-        t_total += time.perf_counter() - t0
-        s = wl.matrices[i]
-        flops += workloads.ns_alg_flops(s.rows, s.cols, wl.ns_steps)
-        done.append(f"{s.rows}x{s.cols}")
-        if t_total > max_seconds:
-            break
-    desc = f"oracle muon_matrix_step (fp64 numpy, bf16 emulation) on {len(done)} matrices [{', '.join(done)}]"
-    return flops / t_total / 1e12, t_total, desc, cores
+    rate = flops / t_total
+    full = workloads.workload_alg_flops(wl) / rate
+    desc = (f"oracle muon_matrix_step (fp64 numpy, bf16 emulation) on {len(done)} matrices "
+            f"[{', '.join(done)}] of the {wl.name} table; the whole table's NS flops at this rate "
+            f"(extrapolated) take {full:.0f} s per step")
+    return {"value": rate / 1e12, "seconds": t_total, "sample": desc, "cores": cores,
+            "extrapolated_step_s": full}
+
+
+def host_mem_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
 
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
-    import torch
-    import matrix_optimizers_zero_gb300 as mo
-    from matrix_optimizers_zero_gb300 import build as mo_build, workloads
+class Owner:
+    """One owner's state on the device: the Muon table (W, G, V), an RMNP copy
+    (its own W and V, the same G) and the AdamW tail, each in one flat
+    buffer with per-tensor views, plus the library tables and workspace."""
 
-    mo_build.build()
-    mo.load_library()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    wl = workloads.get_workload(args.config)
-    peaks = load_peaks()
+    def __init__(self, mo, wl, dev, seed):
+        import torch
+        self.mo, self.wl, self.dev = mo, wl, dev
+        self.shapes = [(s.rows, s.cols) for s in wl.matrices]
+        self.offs, tot = [], 0
+        for r, c in self.shapes:
+            self.offs.append(tot)
+            tot += ((r * c + 63) // 64) * 64
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+        self.Wf = torch.randn(tot, generator=gen, device=dev).mul_(wl.w_std)
+        self.Gf = torch.randn(tot, generator=gen, device=dev).mul_(wl.g_std).to(torch.bfloat16)
+        self.Vf = torch.randn(tot, generator=gen, device=dev).mul_(1e-3)
+        self.Wr = self.Wf.clone()
+        self.Vr = self.Vf.clone()
+        self.W_l, self.G_l, self.V_l = self.views(self.Wf), self.views(self.Gf), self.views(self.Vf)
+        self.Wr_l, self.Vr_l = self.views(self.Wr), self.views(self.Vr)
+        self.muon_tbl = mo.MuonTable(list(zip(self.W_l, self.G_l, self.V_l)))
+        self.rmnp_tbl = mo.MuonTable(list(zip(self.Wr_l, self.G_l, self.Vr_l)))
+        self.tail_sizes = [t for t in wl.tail if t > 0]
+        self.toffs, ttot = [], 0
+        for t in self.tail_sizes:
+            self.toffs.append(ttot)
+            ttot += ((t + 63) // 64) * 64
+        self.Pf = torch.randn(max(ttot, 1), generator=gen, device=dev).mul_(wl.tail_p_std)
+        self.Tg = torch.randn(max(ttot, 1), generator=gen, device=dev).mul_(wl.tail_g_std)
+        self.Tm = torch.zeros(max(ttot, 1), device=dev)
+        self.Tv = torch.zeros(max(ttot, 1), device=dev)
+        self.tail_tbl = self.tail_table(self.Tg)
+        self.mp = mo.MuonParams(lr=wl.lr, wd=wl.wd, mu=wl.mu, ns_steps=wl.ns_steps)
+        self.rp = mo.RmnpParams(lr=wl.lr, wd=wl.wd, mu=wl.mu)
+        self.ws = mo.muon_workspace(self.muon_tbl, self.mp, device=dev)
+        self.adam_step = 0
 
-    # ---- state: flat device buffers with per-matrix views (one copy each for e2e)
-    shapes = [(s.rows, s.cols) for s in wl.matrices]
-    offs, tot = [], 0
-    for r, c in shapes:
-        offs.append(tot)
-        tot += ((r * c + 63) // 64) * 64
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1234 + rank)
-    Wf = torch.randn(tot, generator=gen, device=dev).mul_(wl.w_std)
-    Gf = torch.randn(tot, generator=gen, device=dev).mul_(wl.g_std).to(torch.bfloat16)
-    Vf = torch.randn(tot, generator=gen, device=dev).mul_(1e-3)
-    Wr = Wf.clone()
-    Vr = Vf.clone()
+    def views(self, flat):
+        return [flat[o:o + r * c].view(r, c) for o, (r, c) in zip(self.offs, self.shapes)]
 
-    def views(flat):
-        return [flat[o:o + r * c].view(r, c) for o, (r, c) in zip(offs, shapes)]
+    def tail_table(self, g_flat):
+        return self.mo.TailTable([(self.Pf[o:o + t], g_flat[o:o + t], self.Tm[o:o + t], self.Tv[o:o + t])
+                                  for o, t in zip(self.toffs, self.tail_sizes)])
 
-    W_l, G_l, V_l, Wr_l, Vr_l = views(Wf), views(Gf), views(Vf), views(Wr), views(Vr)
-    muon_tbl = mo.MuonTable(list(zip(W_l, G_l, V_l)))
-    rmnp_tbl = mo.MuonTable(list(zip(Wr_l, G_l, Vr_l)))
-    tail_sizes = [t for t in wl.tail if t > 0]
-    toffs, ttot = [], 0
-    for t in tail_sizes:
-        toffs.append(ttot)
-        ttot += ((t + 63) // 64) * 64
-    Pf = torch.randn(max(ttot, 1), generator=gen, device=dev).mul_(wl.tail_p_std)
-    Tg = torch.randn(max(ttot, 1), generator=gen, device=dev).mul_(wl.tail_g_std)
-    Tm = torch.zeros(max(ttot, 1), device=dev)
-    Tv = torch.zeros(max(ttot, 1), device=dev)
-    segs = [(Pf[o:o + t], Tg[o:o + t], Tm[o:o + t], Tv[o:o + t]) for o, t in zip(toffs, tail_sizes)]
-    tail_tbl = mo.TailTable(segs)
+    def launches_per_step(self):
+        """Kernel launches of one step: the prologue, 3 GEMM launches per
+        iteration (plus one Gram reduction per iteration when a matrix has
+        more than 32768 columns on its long side), AdamW one per 256 segments,
+        RMNP one per 512 entries separately for rows shorter / not shorter
+        than 8192 elements."""
+        wl = self.wl
+        n_long = sum(1 for _, c in self.shapes if c >= 8192)
+        reduce = 1 if any(max(r, c) > 32768 for r, c in self.shapes) else 0
+        return ((1 + (3 + reduce) * wl.ns_steps) + math.ceil(len(self.tail_sizes) / 256)
+                + math.ceil((len(self.shapes) - n_long) / 512) + math.ceil(n_long / 512))
 
-    mp = mo.MuonParams(lr=wl.lr, wd=wl.wd, mu=wl.mu, ns_steps=wl.ns_steps)
-    rp = mo.RmnpParams(lr=wl.lr, wd=wl.wd, mu=wl.mu)
-    ws = mo.muon_workspace(muon_tbl, mp, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    lib = mo.load_library()
-    import ctypes
-    ws_ptr, ws_bytes = ws.data_ptr(), ws.numel()
-    sptr = stream.cuda_stream
-    adam_step = [0]
-    # NVTX ranges name each library call on the host timeline (ncu --nvtx
-    # can filter on them); they add no device work
-    nvtx = torch.cuda.nvtx
-
-    def step(ev=None, tabs=None, between=None):
+    def step(self, stream, ev=None, tabs=None, between=None):
         """One optimizer step on `stream`: Muon, AdamW on the tail, RMNP.
-        tabs: (muon, rmnp, tail) tables to use (default: the resident ones);
-        between: called after the Muon call, before AdamW and RMNP."""
-        m_tbl, r_tbl, t_tbl = tabs if tabs is not None else (muon_tbl, rmnp_tbl, tail_tbl)
+        ev: six events (Muon start, NS start, NS end, Muon end, AdamW end,
+        RMNP end); tabs: (muon, rmnp, tail) tables to use (default: the
+        resident ones); between: called after the Muon call, before AdamW and
+        RMNP."""
+        import ctypes
+        import torch
+        mo, wl = self.mo, self.wl
+        lib = mo.load_library()
+        nvtx = torch.cuda.nvtx      # names each library call on the host timeline; no device work
+        m_tbl, r_tbl, t_tbl = tabs if tabs is not None else (self.muon_tbl, self.rmnp_tbl, self.tail_tbl)
+        sptr = stream.cuda_stream
+        ws_ptr, ws_bytes = self.ws.data_ptr(), self.ws.numel()
         nvtx.range_push("muon_owner_step")
         if ev is None:
-            st = lib.muon_owner_step(m_tbl.ptr, m_tbl.n, ctypes.byref(mp), ws_ptr, ws_bytes, sptr)
+            st = lib.muon_owner_step(m_tbl.ptr, m_tbl.n, ctypes.byref(self.mp), ws_ptr, ws_bytes, sptr)
         else:
             ev[0].record(stream)
-            st = lib.muon_owner_step_timed(muon_tbl.ptr, muon_tbl.n, ctypes.byref(mp), ws_ptr, ws_bytes, sptr,
+            st = lib.muon_owner_step_timed(m_tbl.ptr, m_tbl.n, ctypes.byref(self.mp), ws_ptr, ws_bytes, sptr,
                                            ev[1].cuda_event, ev[2].cuda_event)
         nvtx.range_pop()
         if st != 0:
@@ -265,9 +334,9 @@ def run_ours(args, rank, world, local_rank):
             ev[3].record(stream)
         if between is not None:
             between()
-        adam_step[0] += 1
+        self.adam_step += 1
         ap = mo.AdamWParams(lr=wl.adam_lr, wd=wl.adam_wd, beta1=wl.beta1, beta2=wl.beta2, eps=wl.adam_eps,
-                            step=adam_step[0])
+                            step=self.adam_step)
         nvtx.range_push("adamw_tail_step")
         st = lib.adamw_tail_step(t_tbl.ptr, t_tbl.n, ctypes.byref(ap), sptr)
         nvtx.range_pop()
@@ -276,13 +345,104 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[4].record(stream)
         nvtx.range_push("rmnp_step")
-        st = lib.rmnp_step(r_tbl.ptr, r_tbl.n, ctypes.byref(rp), sptr)
+        st = lib.rmnp_step(r_tbl.ptr, r_tbl.n, ctypes.byref(self.rp), sptr)
         nvtx.range_pop()
         if st != 0:
             raise mo.MoError(st, "rmnp_step")
         if ev is not None:
             ev[5].record(stream)
 
+
+def timed_steps(owner, stream, dev, steps, barrier, clocks=None):
+    """Times `steps` whole steps with CUDA events on `stream` (barrier and
+    synchronize on both sides). Returns the total and per-part means/minima
+    in ms."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for e in evs:
+        for x in e:
+            x.record(stream)          # torch creates events lazily: force the handles to exist
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    if clocks is not None:
+        clocks.mark("begin")
+    t_start.record(stream)
+    for k in range(steps):
+        owner.step(stream, evs[k])
+    t_end.record(stream)
+    barrier()
+    if clocks is not None:
+        clocks.mark("end")
+    total_ms = t_start.elapsed_time(t_end)
+    return {
+        "total_ms": total_ms,
+        "ms_step": total_ms / steps,
+        "pro_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+        "ns_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+        "muon_ms": statistics.mean(e[0].elapsed_time(e[3]) for e in evs),
+        "adam_ms": statistics.mean(e[3].elapsed_time(e[4]) for e in evs),
+        "rmnp_ms": statistics.mean(e[4].elapsed_time(e[5]) for e in evs),
+        "step_min_ms": min(e[0].elapsed_time(e[5]) for e in evs),
+        "ns_min_ms": min(e[1].elapsed_time(e[2]) for e in evs),
+    }
+
+
+def breakdown(wl, t, peaks, steps):
+    """Per-part figures of a timed run: ms, TFLOP/s and GB/s at the
+    algorithmic work counts, and the NS fraction of the bf16 peak chosen by
+    the length of the timed region."""
+    from matrix_optimizers_zero_gb300 import workloads
+    shapes = [(s.rows, s.cols) for s in wl.matrices]
+    ns_flops = workloads.workload_alg_flops(wl)
+    ns_dense = sum(workloads.ns_dense_flops(r, c, wl.ns_steps) for r, c in shapes)
+    n_el = wl.n_elements
+    ns_tflops = ns_flops / (t["ns_ms"] * 1e-3) / 1e12
+    rmnp_gbs = n_el * workloads.RMNP_BYTES_PER_EL / (t["rmnp_ms"] * 1e-3) / 1e9
+    adam_gbs = wl.tail_elements * workloads.ADAMW_BYTES_PER_EL / (t["adam_ms"] * 1e-3) / 1e9
+    pro_gbs = n_el * workloads.PROLOGUE_BYTES_PER_EL / (t["pro_ms"] * 1e-3) / 1e9
+    region_s = t["total_ms"] * 1e-3
+    peak, peak_name = choose_peak(peaks, region_s)
+    return {
+        "muon_step_ms": round(t["muon_ms"], 4),
+        "prologue_ms": round(t["pro_ms"], 4),
+        "prologue_gbs": round(pro_gbs, 1),
+        "prologue_frac_hbm": round(pro_gbs / peaks["hbm_gbs"], 4),
+        "prologue_bytes_per_el": workloads.PROLOGUE_BYTES_PER_EL,
+        "ns_ms": round(t["ns_ms"], 4),
+        "ns_tflops_alg": round(ns_tflops, 2),
+        "ns_tflops_dense_equiv": round(ns_dense / (t["ns_ms"] * 1e-3) / 1e12, 2),
+        "ns_frac_of_peak": round(ns_tflops / peak, 4),
+        "ns_frac_of_burst_peak": round(ns_tflops / peaks["bf16_tflops"], 4),
+        "ns_frac_of_sustained_peak": round(ns_tflops / peaks["bf16_tflops_sustained"], 4),
+        "peak_used": peak_name,
+        "timed_region_s": round(region_s, 3),
+        "adamw_ms": round(t["adam_ms"], 4),
+        "adamw_gbs": round(adam_gbs, 1),
+        "adamw_frac_hbm": round(adam_gbs / peaks["hbm_gbs"], 4),
+        "adamw_elements": wl.tail_elements,
+        "rmnp_ms": round(t["rmnp_ms"], 4),
+        "rmnp_gbs": round(rmnp_gbs, 1),
+        "rmnp_frac_hbm": round(rmnp_gbs / peaks["hbm_gbs"], 4),
+        "means_over_steps": steps,
+        "step_min_ms": round(t["step_min_ms"], 4),
+        "ns_min_ms": round(t["ns_min_ms"], 4),
+        "ns_tflops_alg_best": round(ns_flops / (t["ns_min_ms"] * 1e-3) / 1e12, 2),
+    }
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import matrix_optimizers_zero_gb300 as mo
+    from matrix_optimizers_zero_gb300 import build as mo_build, workloads
+
+    mo_build.build()
+    mo.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -292,9 +452,57 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    wl = workloads.get_workload(args.config)
+    out = headline(args, mo, workloads, wl, dev, stream, peaks, rank, world, local_rank, barrier)
+    time_secondary = args.secondary and args.config != SECONDARY_CONFIG
+    if time_secondary or args.extras:
+        torch.cuda.empty_cache()
+        wl2 = workloads.get_workload(SECONDARY_CONFIG)
+        owner2 = Owner(mo, wl2, dev, 4321 + rank)
+        for _ in range(args.warmup):
+            owner2.step(stream)
+        torch.cuda.synchronize(dev)
+        if time_secondary:
+            t2 = timed_steps(owner2, stream, dev, args.secondary_steps, barrier)
+            if mo.mo_last_device_error() != 0:
+                raise RuntimeError("device-side timeout in the secondary workload")
+            sec = breakdown(wl2, t2, peaks, args.secondary_steps)
+            sec["ms_per_step"] = round(t2["ms_step"], 4)
+            sec["workload"] = (f"{wl2.name}: {len(wl2.matrices)} matrices, {wl2.n_elements} elements, "
+                               f"tail {wl2.tail_elements}")
+            sec["value_tflops_alg_per_step"] = round(
+                workloads.workload_alg_flops(wl2) / (t2["ms_step"] * 1e-3) / 1e12, 2)
+            sec["note"] = ("the pages' own matrix set (GPT-2 Large); the AdamW tail here is L2- and "
+                           "latency-bound and not graded")
+            traffic, how = ns_traffic(wl2.name)
+            sec["ns_traffic_bytes"] = traffic
+            sec["ns_traffic_note"] = how
+            if out is not None:
+                out["secondary"] = {wl2.name: sec}
+        if args.extras:
+            ex = measure_extras(args, mo, workloads, wl2, owner2.shapes, owner2.W_l, owner2.G_l, owner2.V_l,
+                                owner2.Wr_l, owner2.Vr_l, dev, stream, peaks)
+            if out is not None:
+                out["extras"] = {"workload": wl2.name, **ex}
+        del owner2
+    if out is not None and not args.no_cpu_baseline:
+        cb = cpu_oracle_sample(wl, max_seconds=args.cpu_seconds, min_seconds=10.0)
+        out["cpu_baseline"] = {"value": round(cb["value"], 6), "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+                               "sample": cb["sample"], "seconds": round(cb["seconds"], 2),
+                               "extrapolated_step_s": round(cb["extrapolated_step_s"], 1)}
+    return out
+
+
+def headline(args, mo, workloads, wl, dev, stream, peaks, rank, world, local_rank, barrier):
+    """The headline line for workload `wl`: the device-resident timed run,
+    then the end-to-end run through the C ABI with host buffers."""
+    import torch
+    owner = Owner(mo, wl, dev, 1234 + rank)
+    shapes = owner.shapes
+
     # ---- warmup
     for _ in range(args.warmup):
-        step()
+        owner.step(stream)
     torch.cuda.synchronize(dev)
     if mo.mo_last_device_error() != 0:
         raise RuntimeError("device-side timeout during warmup")
@@ -303,149 +511,24 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     clocks.start()
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    for e in evs:
-        for x in e:
-            x.record(stream)          # torch creates events lazily: force the handles to exist
-    torch.cuda.synchronize(dev)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    barrier()
-    clocks.mark("begin")
-    t_start.record(stream)
-    for k in range(args.steps):
-        step(evs[k])
-    t_end.record(stream)
-    barrier()
-    clocks.mark("end")
+    t = timed_steps(owner, stream, dev, args.steps, barrier, clocks)
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    ms_step = total_ms / args.steps
-    pro_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    ns_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    muon_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in evs)
-    adam_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
-    rmnp_ms = statistics.mean(e[4].elapsed_time(e[5]) for e in evs)
-    # per-step minima (each step's events from its Muon start to its RMNP end)
-    step_min_ms = min(e[0].elapsed_time(e[5]) for e in evs)
-    ns_min_ms = min(e[1].elapsed_time(e[2]) for e in evs)
-
+    ms_max = max_over_ranks(t["ms_step"], dev)
     ns_flops = workloads.workload_alg_flops(wl)
-    ns_dense = sum(workloads.ns_dense_flops(r, c, wl.ns_steps) for r, c in shapes)
-    n_el = wl.n_elements
-    ns_tflops = ns_flops / (ns_ms * 1e-3) / 1e12
-    rmnp_gbs = n_el * workloads.RMNP_BYTES_PER_EL / (rmnp_ms * 1e-3) / 1e9
-    adam_gbs = wl.tail_elements * workloads.ADAMW_BYTES_PER_EL / (adam_ms * 1e-3) / 1e9
-    pro_gbs = n_el * 16 / (pro_ms * 1e-3) / 1e9
-
-    ms_max = max_over_ranks(ms_step, dev)
     value = whole_job_tflops(world, ns_flops, ms_max)
+    bd = breakdown(wl, t, peaks, args.steps)
 
-    # ---- end to end through the C ABI with host buffers. Every step uploads
-    # its gradients (Muon/RMNP G and the tail's g) from pinned host memory and
-    # reads all updated weights back (Muon W, RMNP W, tail p). Uploads, compute
-    # and read-backs run on three streams: the gradients are double-buffered on
-    # the device so step k+1's upload overlaps step k; a step's Muon call waits
-    # until the previous step's Muon weights have been read back, its AdamW
-    # and RMNP calls until the previous RMNP weights and tail have been.
-    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 10))
-    pin = e2e_steps > 0
-    hG = torch.empty(Gf.numel() if pin else 1, dtype=torch.bfloat16, pin_memory=pin)
-    hTg = torch.empty(Tg.numel() if pin else 1, dtype=torch.float32, pin_memory=pin)
-    hW = torch.empty(Wf.numel() if pin else 1, dtype=torch.float32, pin_memory=pin)
-    hWr = torch.empty(Wr.numel() if pin else 1, dtype=torch.float32, pin_memory=pin)
-    hP = torch.empty(Pf.numel() if pin else 1, dtype=torch.float32, pin_memory=pin)
-    h2d = hG.numel() * 2 + hTg.numel() * 4
-    d2h = hW.numel() * 4 + hWr.numel() * 4 + hP.numel() * 4
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    if pin:
-        hG.copy_(Gf)
-        hTg.copy_(Tg)
-        Gf2, Tg2 = torch.empty_like(Gf), torch.empty_like(Tg)
-        G2_l = views(Gf2)
-        segs2 = [(Pf[o:o + t], Tg2[o:o + t], Tm[o:o + t], Tv[o:o + t]) for o, t in zip(toffs, tail_sizes)]
-        bufs = [(Gf, Tg, (muon_tbl, rmnp_tbl, tail_tbl)),
-                (Gf2, Tg2, (mo.MuonTable(list(zip(W_l, G2_l, V_l))), mo.MuonTable(list(zip(Wr_l, G2_l, Vr_l))),
-                            mo.TailTable(segs2)))]
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event(), torch.cuda.Event()]
-        ev_free = [torch.cuda.Event(), torch.cuda.Event()]
-        ev_w, ev_wout, ev_r, ev_rout = (torch.cuda.Event() for _ in range(4))
-        step(tabs=bufs[1][2])               # plan the second tables outside the timed region
-        torch.cuda.synchronize(dev)
-        barrier()
-        e0.record(stream)
-        s_in.wait_event(e0)
-        s_out.wait_event(e0)
-        for k in range(e2e_steps):
-            b = k % 2
-            Gd, Tgd, tabs = bufs[b]
-            if k >= 2:
-                s_in.wait_event(ev_free[b])   # step k-2 no longer reads buffer b
-            with torch.cuda.stream(s_in):
-                Gd.copy_(hG, non_blocking=True)
-                Tgd.copy_(hTg, non_blocking=True)
-            ev_in[b].record(s_in)
-            stream.wait_event(ev_in[b])
-            if k >= 1:
-                stream.wait_event(ev_wout)
-
-            def after_muon():
-                ev_w.record(stream)
-                if k >= 1:
-                    stream.wait_event(ev_rout)
-
-            step(tabs=tabs, between=after_muon)
-            ev_r.record(stream)
-            ev_free[b].record(stream)
-            s_out.wait_event(ev_w)
-            with torch.cuda.stream(s_out):
-                hW.copy_(Wf, non_blocking=True)
-            ev_wout.record(s_out)
-            s_out.wait_event(ev_r)
-            with torch.cuda.stream(s_out):
-                hWr.copy_(Wr, non_blocking=True)
-                hP.copy_(Pf, non_blocking=True)
-            ev_rout.record(s_out)
-        stream.wait_event(ev_rout)
-        e1.record(stream)
-    else:
-        e0.record(stream)
-        e1.record(stream)
-    barrier()
-    e2e_ms_max = max_over_ranks(e0.elapsed_time(e1) / max(e2e_steps, 1), dev)
-    e2e_value = whole_job_tflops(world, ns_flops, e2e_ms_max)
-    # the host link as this run sees it: one plain pinned copy each way, so a
-    # link-bound e2e figure can be read against what the link delivered
-    link = None
-    if pin:
-        l0, l1, l2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        with torch.cuda.stream(s_out):
-            l0.record(s_out)
-            hW.copy_(Wf, non_blocking=True)
-            l1.record(s_out)
-            Gf.copy_(hG, non_blocking=True)
-            l2.record(s_out)
-        l2.synchronize()
-        link = {"d2h_gbs": round(hW.numel() * 4 / (l0.elapsed_time(l1) * 1e-3) / 1e9, 1),
-                "h2d_gbs": round(hG.numel() * 2 / (l1.elapsed_time(l2) * 1e-3) / 1e9, 1)}
+    e2e = end_to_end(args, mo, owner, dev, stream, barrier, world, ns_flops)
     if mo.mo_last_device_error() != 0:
         raise RuntimeError("device-side timeout during the timed region")
-
-    extras = measure_extras(args, mo, workloads, wl, shapes, W_l, G_l, V_l, Wr_l, Vr_l, dev, stream, peaks) \
-        if args.extras else None
 
     if rank != 0:
         return None
 
-    # prologue + 3 GEMM launches per iteration; AdamW: one per 256 segments;
-    # RMNP: one per 512 entries, separately for rows shorter / not shorter
-    # than 8192 elements (warp-per-row and CTA-per-row kernels)
-    n_long = sum(1 for _, c in shapes if c >= 8192)
-    launches_per_step = ((1 + 3 * wl.ns_steps) + math.ceil(len(tail_sizes) / 256)
-                         + math.ceil((len(shapes) - n_long) / 512) + math.ceil(n_long / 512))
-    peak = peaks["bf16_tflops_sustained"]
+    ns_tflops = bd["ns_tflops_alg"]
+    peak, peak_name = choose_peak(peaks, t["total_ms"] * 1e-3)
+    traffic, traffic_note = ns_traffic(wl.name)
+    n_el = wl.n_elements
     out = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -468,23 +551,7 @@ def run_ours(args, rank, world, local_rank):
             "parallelism": f"replicas x{world}",
             "state": "fp32 W/V, bf16 G; NS operands bf16 with fp32 accumulation",
         },
-        "breakdown": {
-            "muon_step_ms": round(muon_ms, 4),
-            "prologue_ms": round(pro_ms, 4),
-            "prologue_gbs": round(pro_gbs, 1),
-            "ns_ms": round(ns_ms, 4),
-            "ns_tflops_alg": round(ns_tflops, 2),
-            "ns_tflops_dense_equiv": round(ns_dense / (ns_ms * 1e-3) / 1e12, 2),
-            "adamw_ms": round(adam_ms, 4),
-            "adamw_gbs": round(adam_gbs, 1),
-            "rmnp_ms": round(rmnp_ms, 4),
-            "rmnp_gbs": round(rmnp_gbs, 1),
-            "rmnp_frac_hbm": round(rmnp_gbs / peaks["hbm_gbs"], 4),
-            "means_over_steps": args.steps,
-            "step_min_ms": round(step_min_ms, 4),
-            "ns_min_ms": round(ns_min_ms, 4),
-            "ns_tflops_alg_best": round(ns_flops / (ns_min_ms * 1e-3) / 1e12, 2),
-        },
+        "breakdown": bd,
         "roofline": {
             "bound": "tensor",
             "kernel": "ns_gemm_pair_kernel (the 15 Gram, A.A and B.X launches of one step)",
@@ -492,25 +559,119 @@ def run_ours(args, rank, world, local_rank):
             "peak": peak,
             "unit": "TFLOP/s",
             "frac": round(ns_tflops / peak, 4),
-            "traffic": ns_traffic(wl.name),
-            "traffic_unit": "DRAM bytes per step's 15 NS launches (ncu, full table, single-pass metrics)",
-            "peak_source": f"bf16_tflops_sustained ({peaks['source']})",
+            "traffic": traffic,
+            "traffic_unit": "DRAM bytes per step's 15 NS launches",
+            "traffic_note": traffic_note,
+            "peak_source": f"{peak_name} ({peaks['source']}); timed region {t['total_ms'] * 1e-3:.2f} s",
+            "frac_of_burst_peak": bd["ns_frac_of_burst_peak"],
+            "frac_of_sustained_peak": bd["ns_frac_of_sustained_peak"],
         },
-        "e2e": ({"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms_max, 3), "steps": e2e_steps,
-                 "link_measured": link,
-                 "copies": "pinned host buffers; uploads, compute and read-backs on three streams, "
-                           "gradients double-buffered on the device"}
-                if e2e_steps else None),
-        "gpu_launches": int(launches_per_step * args.steps),
-        **({"extras": extras} if extras is not None else {}),
+        "e2e": e2e,
+        "gpu_launches": int(owner.launches_per_step() * args.steps),
         "clocks": clk,
     }
-    if not args.no_cpu_baseline:
-        v, secs, desc, cores = cpu_oracle_sample(wl, max_seconds=args.cpu_seconds, min_seconds=10.0)
-        out["cpu_baseline"] = {"value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                               "sample": desc, "seconds": round(secs, 2)}
     return out
+
+
+def end_to_end(args, mo, owner, dev, stream, barrier, world, ns_flops):
+    """The same step through the C ABI with host buffers. Every step uploads
+    its gradients (Muon/RMNP G and the tail's g) from pinned host memory and
+    reads all updated weights back (Muon W, RMNP W, tail p). Uploads, compute
+    and read-backs run on three streams: the gradients are double-buffered on
+    the device so step k+1's upload overlaps step k; a step's Muon call waits
+    until the previous step's Muon weights have been read back, its AdamW and
+    RMNP calls until the previous RMNP weights and tail have been."""
+    import torch
+    if args.no_e2e:
+        return None
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    need = owner.Gf.numel() * 2 + owner.Tg.numel() * 4 + (owner.Wf.numel() + owner.Wr.numel() + owner.Pf.numel()) * 4
+    avail = host_mem_available_bytes()
+    if avail is not None and need > 0.7 * avail:
+        return {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "unavailable": f"pinned host buffers need {need / 1e9:.1f} GB, host has {avail / 1e9:.1f} GB available"}
+    t_pin = time.perf_counter()
+    hG = torch.empty(owner.Gf.numel(), dtype=torch.bfloat16, pin_memory=True)
+    hTg = torch.empty(owner.Tg.numel(), dtype=torch.float32, pin_memory=True)
+    hW = torch.empty(owner.Wf.numel(), dtype=torch.float32, pin_memory=True)
+    hWr = torch.empty(owner.Wr.numel(), dtype=torch.float32, pin_memory=True)
+    hP = torch.empty(owner.Pf.numel(), dtype=torch.float32, pin_memory=True)
+    pin_s = time.perf_counter() - t_pin
+    h2d = hG.numel() * 2 + hTg.numel() * 4
+    d2h = hW.numel() * 4 + hWr.numel() * 4 + hP.numel() * 4
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    hG.copy_(owner.Gf)
+    hTg.copy_(owner.Tg)
+    Gf, Tg = owner.Gf, owner.Tg
+    Gf2, Tg2 = torch.empty_like(Gf), torch.empty_like(Tg)
+    mo_ = owner.mo
+    bufs = [(Gf, Tg, (owner.muon_tbl, owner.rmnp_tbl, owner.tail_tbl)),
+            (Gf2, Tg2, (mo_.MuonTable(list(zip(owner.W_l, owner.views(Gf2), owner.V_l))),
+                        mo_.MuonTable(list(zip(owner.Wr_l, owner.views(Gf2), owner.Vr_l))),
+                        owner.tail_table(Tg2)))]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_free = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_w, ev_wout, ev_r, ev_rout = (torch.cuda.Event() for _ in range(4))
+    owner.step(stream, tabs=bufs[1][2])     # plan the second tables outside the timed region
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for k in range(e2e_steps):
+        b = k % 2
+        Gd, Tgd, tabs = bufs[b]
+        if k >= 2:
+            s_in.wait_event(ev_free[b])   # step k-2 no longer reads buffer b
+        with torch.cuda.stream(s_in):
+            Gd.copy_(hG, non_blocking=True)
+            Tgd.copy_(hTg, non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if k >= 1:
+            stream.wait_event(ev_wout)
+
+        def after_muon():
+            ev_w.record(stream)
+            if k >= 1:
+                stream.wait_event(ev_rout)
+
+        owner.step(stream, tabs=tabs, between=after_muon)
+        ev_r.record(stream)
+        ev_free[b].record(stream)
+        s_out.wait_event(ev_w)
+        with torch.cuda.stream(s_out):
+            hW.copy_(owner.Wf, non_blocking=True)
+        ev_wout.record(s_out)
+        s_out.wait_event(ev_r)
+        with torch.cuda.stream(s_out):
+            hWr.copy_(owner.Wr, non_blocking=True)
+            hP.copy_(owner.Pf, non_blocking=True)
+        ev_rout.record(s_out)
+    stream.wait_event(ev_rout)
+    e1.record(stream)
+    barrier()
+    e2e_ms_max = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_value = whole_job_tflops(world, ns_flops, e2e_ms_max)
+    # the host link as this run sees it: one plain pinned copy each way, so a
+    # link-bound e2e figure can be read against what the link delivered
+    l0, l1, l2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    with torch.cuda.stream(s_out):
+        l0.record(s_out)
+        hW.copy_(owner.Wf, non_blocking=True)
+        l1.record(s_out)
+        Gf.copy_(hG, non_blocking=True)
+        l2.record(s_out)
+    l2.synchronize()
+    link = {"d2h_gbs": round(hW.numel() * 4 / (l0.elapsed_time(l1) * 1e-3) / 1e9, 1),
+            "h2d_gbs": round(hG.numel() * 2 / (l1.elapsed_time(l2) * 1e-3) / 1e9, 1)}
+    return {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms_max, 3), "steps": e2e_steps,
+            "link_measured": link, "pinned_alloc_s": round(pin_s, 1),
+            "copies": "pinned host buffers; uploads, compute and read-backs on three streams, "
+                      "gradients double-buffered on the device"}
 
 
 # ---------------------------------------------------------------- next-row kernels (--extras)
@@ -643,35 +804,42 @@ def measure_extras(args, mo, workloads, wl, shapes, W_l, G_l, V_l, Wr_l, Vr_l, d
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args, rank):
+    """The CPU oracle as it stands, on the host cores: each step is one
+    whole-matrix Muon step of the oracle on a matrix of the workload, cycling
+    through the distinct shapes whose oracle step costs at most three times
+    the cheapest one (a bounded sample: the 8B table's largest matrices take
+    the oracle about half a minute each)."""
     if rank != 0:
         return None
     from matrix_optimizers_zero_gb300 import workloads
     wl = workloads.get_workload(args.config)
-    seen, picks = set(), []
-    for i, s in enumerate(wl.matrices):
-        if (s.rows, s.cols) not in seen:
-            seen.add((s.rows, s.cols))
-            picks.append(i)
+    by_cost = distinct_shapes_by_cost(wl)
+
+    def cost(i):
+        return workloads.ns_alg_flops(wl.matrices[i].rows, wl.matrices[i].cols, wl.ns_steps)
+
+    picks = [i for i in by_cost if cost(i) <= 3 * cost(by_cost[0])]
     cores = len(os.sched_getaffinity(0))
     for k in range(args.warmup):
-        cpu_oracle_sample(wl, max_seconds=0.0, indices=[picks[k % len(picks)]])
+        oracle_matrix_seconds(wl, picks[k % len(picks)])
     times, flops = [], 0
     for k in range(args.steps):
-        i = picks[k % len(picks)]
-        v, secs, _, _ = cpu_oracle_sample(wl, max_seconds=0.0, indices=[i])
-        s = wl.matrices[i]
+        secs, f = oracle_matrix_seconds(wl, picks[k % len(picks)])
         times.append(secs)
-        flops += workloads.ns_alg_flops(s.rows, s.cols, wl.ns_steps)
+        flops += f
     total = sum(times)
     value = flops / total / 1e12
-    desc = (f"each step: the oracle's whole-matrix Muon step on one matrix of the {wl.name} table, cycling "
-            f"through its {len(picks)} distinct shapes")
+    shapes = ", ".join(f"{wl.matrices[i].rows}x{wl.matrices[i].cols}" for i in picks)
+    desc = (f"each step: the oracle's whole-matrix Muon step (fp64 numpy, bf16 emulation) on one matrix of "
+            f"the {wl.name} table, cycling through the shapes [{shapes}]")
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name} (bounded sample per step)", "l2": "n/a (CPU)"},
+        "config": {"workload": f"{wl.name}: {len(wl.matrices)} matrices, {wl.n_elements} elements, "
+                               f"tail {wl.tail_elements}",
+                   "sample": "bounded sample per step (see cpu_baseline)", "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -683,12 +851,17 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="gpt2l")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--cpu-seconds", type=float, default=25.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop (profiling runs)")
+    ap.add_argument("--e2e-steps", type=int, default=10, help="end-to-end steps (at most --steps)")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false",
+                    help=f"skip the second workload ({SECONDARY_CONFIG}) timed after the headline")
+    ap.add_argument("--secondary-steps", type=int, default=20)
     ap.add_argument("--extras", action="store_true",
-                    help="also time the next-row kernels (Muon variants, column-cut RMNP, HTRMNP, planner)")
+                    help=f"also time the next-row kernels on the {SECONDARY_CONFIG} table (Muon variants, "
+                         "column-cut RMNP, HTRMNP, graph replay, planner)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -132,6 +132,15 @@ def get_workload(name: str) -> Workload:
     if name == "llama8b":
         m, t = _llama8b()
         return Workload("llama8b", 2, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
+    if name == "llama8b_1layer":
+        # one layer of the Llama-style 8B set (7 matrices, 218 M elements) and a
+        # tail of its two RMSNorm vectors plus one eighth of the embedding
+        # (65.7 M elements, 1.05 GB of AdamW state): the same kernels on a
+        # ~5 GB working set, every buffer still larger than L2; used for
+        # profiler captures, whose traffic scales by 32 to the full table
+        m, t = _llama8b()
+        return Workload("llama8b_1layer", 6, m[:7], (4096, 4096, 128256 * 512), w_std=0.02, g_std=1e-3,
+                        tail_p_std=0.02, tail_g_std=1e-3)
     if name == "spectrum":
         m, t = _spectrum()
         return Workload("spectrum", 3, m, t, w_std=0.02, g_std=1.0, tail_p_std=0.02, tail_g_std=1e-3)
@@ -293,7 +302,8 @@ def ns_dense_flops(rows: int, cols: int, steps: int = 5) -> int:
 
 
 # algorithmic HBM bytes per element
-MUON_NONGEMM_BYTES_PER_EL = 20   # G 2 + V 4+4 + X0 2 (prologue) + W 4+4 (update)
+PROLOGUE_BYTES_PER_EL = 12       # G 2 + V 4+4 + X0 2 (momentum, norm, bf16 cast)
+MUON_NONGEMM_BYTES_PER_EL = 20   # the prologue's 12 + W 4+4 (update)
 RMNP_BYTES_PER_EL = 18           # G 2 + V 4+4 + W 4+4
 ADAMW_BYTES_PER_EL = 28          # p, m, v read + write (24) + g read (4)
 

@@ -22,7 +22,7 @@ Sources (cited by page title and section):
            sqrt(max(1, rows/cols)), the row-normalisation with fp32 sums and
            the 1e-12 clamp of F.normalize).
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
   * The iteration is written as A = X X^T, B = b A + c A A, X' = a X + B X.
     The appendix script writes it as A = X X^T, B = A X, X' = a X + b B + c A B;
     the two are equal in exact arithmetic (a self-check pins this). The
