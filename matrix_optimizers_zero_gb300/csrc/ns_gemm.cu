@@ -303,7 +303,7 @@ constexpr int kPairStages = 6;
 constexpr uint32_t kPairHalfBytes = 128 * kBK * 2;                  // 16 KB
 constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;            // A half + B half
 constexpr uint32_t kPairNumBars = 2 * kPairStages + 5;
-constexpr uint32_t kPairCtrlBytes = 256;                            // barriers, TMEM slot, abort flag
+constexpr uint32_t kPairCtrlBytes = 256;   // barriers; TMEM slot, abort flag, the peer's report (2 words)
 static_assert(8 * kPairNumBars + 16 <= kPairCtrlBytes, "control block");
 constexpr size_t kPairSmem = 1024 + size_t(kPairStages) * kPairStageBytes + kPairCtrlBytes;
 
@@ -319,6 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   const uint32_t bars = base + uint32_t(kPairStages) * kPairStageBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + size_t(kPairStages) * kPairStageBytes + 8 * kPairNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // written by the peer CTA at the end: [0] it gave up, [1] its producer's issued stage count
+  volatile uint32_t* peer_report = tmem_slot + 2;
   auto full_bar = [&](int s) { return bars + 8u * uint32_t(s); };
   auto empty_bar = [&](int s) { return bars + 8u * uint32_t(kPairStages + s); };
   auto tfull_bar = [&](int s) { return bars + 8u * uint32_t(2 * kPairStages + s); };
@@ -343,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
     }
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
+    peer_report[0] = 0u;
+    peer_report[1] = 0u;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -359,11 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
+  uint32_t n_issued = 0;      // producer: operand stages issued (stage j % S, phase parity (j / S) & 1)
+  bool mma_issued = false;    // MMA issuer: any MMA issued
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer (both CTAs)
-      int32_t pending[kPairStages];
-      for (int s = 0; s < kPairStages; ++s) pending[s] = -1;
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -422,22 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
             ptx::tma_load_2d_pair(sb, mapB, fb, bcol, k0);
             ptx::tma_load_2d_pair(sb + kBoxBytes, mapB, fb, bcol + 64, k0);
           }
-          pending[stage] = int32_t(ph);
+          ++n_issued;
           if (++stage == kPairStages) {
             stage = 0;
             ph ^= 1u;
-          }
-        }
-      }
-      if (*abort_flag) {
-        if (leader) {
-          // the leader's full barriers count both CTAs' bytes
-          for (int s = 0; s < kPairStages; ++s)
-            if (pending[s] >= 0) mbar_wait_drain(full_bar(s), uint32_t(pending[s]), p.timeout_ns);
-        } else {
-          // the peer cannot observe the leader's barriers: give its copies time to land
-          const uint64_t t0 = ptx::globaltimer_ns();
-          while (ptx::globaltimer_ns() - t0 < 2000000ull) {
           }
         }
       }
@@ -450,7 +442,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
       uint32_t ph = 0;
       int acc = 0;
       uint32_t aph = 0;
-      bool issued = false;
       bool ok = true;
       for (int t = cid; ok && t < p.ntiles; t += ncl) {
         const TileRec tr = p.tiles[t];
@@ -477,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
             ptx::umma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           ptx::umma_commit_pair(empty_bar(stage), 0x3);
-          issued = true;
+          mma_issued = true;
           if (++stage == kPairStages) {
             stage = 0;
             ph ^= 1u;
@@ -487,10 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
         ptx::umma_commit_pair(tfull_bar(acc), 0x3);
         acc ^= 1;
         if (acc == 0) aph ^= 1u;
-      }
-      if (*abort_flag && issued) {
-        ptx::umma_commit_pair(drain_bar, 0x1);
-        mbar_wait_drain(drain_bar, 0u, p.timeout_ns);
       }
     }
   } else {
@@ -525,8 +512,42 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncthreads();   // every role has finished: this CTA's abort flag and issue count are final
+  // Each CTA tells its peer whether it gave up and how many operand stages
+  // its producer issued (thread 0 is the producer lane).
+  if (threadIdx.x == 0)
+    ptx::st_shared_cluster_v2(ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t*>(peer_report)), rank ^ 1u),
+                              *abort_flag != 0 ? 1u : 0u, n_issued);
   ptx::cluster_sync();
+  if (*abort_flag != 0 || peer_report[0] != 0u) {   // the same decision on both CTAs
+    // Nothing may still be writing into either CTA's shared memory or TMEM
+    // when they exit. The even CTA waits for its MMAs, then for every
+    // operand stage either producer left in flight: all copies of both CTAs
+    // count their bytes on the even CTA's full barriers, so it settles each
+    // stage the two producers did not both fill (arming the ones only the
+    // peer filled, completing the peer's share of the ones only it filled)
+    // and waits for the stage's phase. Each producer waits for the MMAs to
+    // consume a stage before refilling it, so the two issue counts differ by
+    // at most S and only the last S stages can be in flight. The second
+    // cluster barrier keeps the odd CTA resident until the drain is over.
+    if (leader && warp == 1 && lane == 0 && mma_issued) {
+      ptx::umma_commit_pair(drain_bar, 0x1);
+      mbar_wait_drain(drain_bar, 0u, p.timeout_ns);
+    }
+    if (leader && threadIdx.x == 0) {
+      const uint32_t L = n_issued, P = peer_report[1];
+      const uint32_t M = L > P ? L : P;
+      for (uint32_t j = M > uint32_t(kPairStages) ? M - uint32_t(kPairStages) : 0u; j < M; ++j) {
+        const int s = int(j % uint32_t(kPairStages));
+        if (j >= L)
+          ptx::mbar_arrive_expect_tx(full_bar(s), kPairStageBytes);   // only the peer's half is coming
+        else if (j >= P)
+          ptx::mbar_complete_tx(full_bar(s), kPairStageBytes);        // the peer's half never will
+        mbar_wait_drain(full_bar(s), (j / uint32_t(kPairStages)) & 1u, p.timeout_ns);
+      }
+    }
+    ptx::cluster_sync();
+  }
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
 }
