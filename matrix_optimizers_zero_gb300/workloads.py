@@ -123,12 +123,12 @@ def get_workload(name: str) -> Workload:
     if name == "gpt2l":
         m, t = _gpt2l()
         return Workload("gpt2l", 1, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
-    if name == "gpt2l_4layers":
-        # four layers of the GPT-2 Large set: the same kernels on a ~2 GB
-        # working set (each bf16 iterate buffer, 157 MB, still exceeds L2);
-        # used for profiler captures
-        m, t = _gpt2l(4)
-        return Workload("gpt2l_4layers", 5, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
+    if name.startswith("gpt2l_") and name.endswith("layers") and name[6:-6].isdigit():
+        # the first N layers of the GPT-2 Large set (gpt2l_4layers: the same
+        # kernels on a ~2 GB working set, each bf16 iterate buffer (157 MB)
+        # still larger than L2; used for profiler captures)
+        m, t = _gpt2l(int(name[6:-6]))
+        return Workload(name, 5, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
     if name == "llama8b":
         m, t = _llama8b()
         return Workload("llama8b", 2, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
@@ -263,6 +263,46 @@ def device_matrices(wl: Workload, device, seed: int = BASE_SEED, v_std: float = 
         else:
             v = torch.zeros(shape, device=device, dtype=torch.float32)
         out.append((w, g, v))
+    return out
+
+
+def _device_haar(gen, rows: int, cols: int, device):
+    """rows x cols (rows >= cols) with orthonormal columns on `device`: QR of
+    a Gaussian matrix with the sign of diag(R) folded in (Haar-distributed),
+    in fp32."""
+    import torch
+    z = torch.randn((rows, cols), generator=gen, device=device, dtype=torch.float32)
+    q, r = torch.linalg.qr(z)
+    return q * torch.sign(torch.diagonal(r))[None, :]
+
+
+def device_structured_matrices(wl: Workload, device, seed: int = BASE_SEED):
+    """W, G, V for every matrix of a table, generated on `device` with the
+    structure its kind states: "haar" G = U diag(s) V^T with Haar U, V and s
+    log-uniform on [1e-4, 1]; "orthorows" G = diag(z^2) Q with orthonormal
+    rows Q and z ~ N(1, 0.3); "normal" G ~ N(0, g_std). W ~ N(0, w_std), V = 0.
+    Used for the structured-spectrum batch at full size, where host QR of
+    every matrix would dominate; the values differ from host_matrix()."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed * 1000003 + wl.config_id + 700)
+    out = []
+    for spec in wl.matrices:
+        r, c = spec.rows, spec.cols
+        k = min(r, c)
+        w = torch.randn((r, c), generator=gen, device=device, dtype=torch.float32).mul_(wl.w_std)
+        if spec.kind == "haar":
+            u = _device_haar(gen, r, k, device)
+            v = _device_haar(gen, c, k, device)
+            s = torch.empty(k, device=device, dtype=torch.float32).uniform_(math.log(1e-4), 0.0, generator=gen).exp_()
+            g = (u * s[None, :]) @ v.T
+        elif spec.kind == "orthorows":
+            q = _device_haar(gen, c, r, device).T          # r x c, orthonormal rows (r <= c)
+            z = torch.randn(r, generator=gen, device=device, dtype=torch.float32).mul_(0.3).add_(1.0)
+            g = (z * z)[:, None] * q
+        else:
+            g = torch.randn((r, c), generator=gen, device=device, dtype=torch.float32).mul_(wl.g_std)
+        out.append((w, g.to(torch.bfloat16).contiguous(), torch.zeros_like(w)))
     return out
 
 

@@ -66,3 +66,45 @@ def fp32_accumulation_noise(X0, O_ref, coeffs, steps):
         X = oracle.bf16_round(Xn.astype(np.float64)).astype(np.float32) if k < steps - 1 else Xn
     X = X.astype(np.float64)
     return rel_frob(X.T if tall else X, O_ref)
+
+
+# ---------------------------------------------------------------- oracle checks in worker processes
+
+def oracle_muon_errors(W0, G0, V0, W1, V1, opts, scale):
+    """(max relative momentum error, relative Frobenius error of the
+    Newton-Schulz direction) of one GPU Muon step: W0/G0/V0 the inputs, W1/V1
+    the GPU's outputs (float32 arrays; G0 holds the bf16 values exactly),
+    `opts` the oracle's keyword arguments, `scale` the update's shape scale."""
+    import oracle
+    W0, G0, V0 = (np.asarray(x, np.float64) for x in (W0, G0, V0))
+    R, C = W0.shape
+    _, Vn, O = oracle.muon_matrix_step(W0, G0, V0, **opts)
+    O_gpu = extract_update(W0, W1, opts["lr"], opts["wd"], R, C, scale)
+    return max_rel(V1, Vn), rel_frob(O_gpu, O)
+
+
+class OraclePool:
+    """Worker processes (spawned, so a CUDA context in the parent is never
+    forked) that run CPU oracle checks of large matrices side by side while
+    the GPU part of a test goes on. The oracle's elementwise bf16 emulation is
+    single-threaded, so several workers with a share of the BLAS threads each
+    finish a batch of matrices ~2.5x sooner than one process. A worker that
+    dies makes every pending result raise instead of waiting."""
+
+    def __init__(self, workers: int = 4):
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        import os
+        import oracle_worker
+        cores = len(os.sched_getaffinity(0))
+        workers = max(1, min(workers, cores))
+        self.ex = cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn"),
+                                         initializer=oracle_worker.init, initargs=(max(1, cores // workers),))
+
+    def muon_errors(self, *args):
+        """A future of oracle_muon_errors(*args) run in a worker."""
+        import oracle_worker
+        return self.ex.submit(oracle_worker.muon_errors, *args)
+
+    def close(self):
+        self.ex.shutdown(wait=True, cancel_futures=True)

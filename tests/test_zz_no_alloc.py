@@ -3,7 +3,8 @@ device memory (for example when a framework's allocator owns the device, or
 in contexts where cudaMalloc is not allowed). It uses the library's fixed
 scratch array instead of a caller workspace; these tests call it through the
 C ABI and check it against muon_owner_step with a caller workspace, on two
-calls in a row, within the parity tolerances of the other GPU tests."""
+calls in a row: within the parity tolerances of the other GPU tests, and
+bit-identical (the same kernels run on the same inputs)."""
 import ctypes
 
 import numpy as np
@@ -45,10 +46,14 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
         torch.cuda.synchronize(DEV)
         assert mo.mo_last_device_error() == 0
         for (Wr, _, Vr), (Wg, _, Vg), w, (R, C) in zip(ref, got, w0, shapes):
+            # within the parity tolerances of the other GPU tests ...
             o_ref = extract_update(w, f64(Wr), p.lr, p.wd, R, C)
             o_got = extract_update(w, f64(Wg), p.lr, p.wd, R, C)
             assert rel_frob(o_got, o_ref) <= NS_REL_FROB_TOL, (call, R, C)
             assert max_rel(f64(Vg), f64(Vr)) <= FP32_MAX_REL_TOL, (call, R, C)
+            # ... and bit-identical: the same kernels and schedule on the same inputs
+            assert torch.equal(Wg, Wr), (call, R, C)
+            assert torch.equal(Vg, Vr), (call, R, C)
 
 
 def test_noalloc_rejects_tables_beyond_the_scratch(lib):
