@@ -457,7 +457,7 @@ def run_ours(args, rank, world, local_rank):
     time_secondary = args.secondary and args.config != SECONDARY_CONFIG
     if time_secondary or args.extras:
         torch.cuda.empty_cache()
-        wl2 = workloads.get_workload(SECONDARY_CONFIG)
+        wl2 = workloads.get_workload(SECONDARY_CONFIG if time_secondary else args.extras_config)
         owner2 = Owner(mo, wl2, dev, 4321 + rank)
         for _ in range(args.warmup):
             owner2.step(stream)
@@ -479,6 +479,11 @@ def run_ours(args, rank, world, local_rank):
             sec["ns_traffic_note"] = how
             if out is not None:
                 out["secondary"] = {wl2.name: sec}
+        if args.extras and wl2.name != args.extras_config:
+            del owner2
+            torch.cuda.empty_cache()
+            wl2 = workloads.get_workload(args.extras_config)
+            owner2 = Owner(mo, wl2, dev, 4321 + rank)
         if args.extras:
             ex = measure_extras(args, mo, workloads, wl2, owner2.shapes, owner2.W_l, owner2.G_l, owner2.V_l,
                                 owner2.Wr_l, owner2.Vr_l, dev, stream, peaks)
@@ -860,8 +865,9 @@ def main():
                     help=f"skip the second workload ({SECONDARY_CONFIG}) timed after the headline")
     ap.add_argument("--secondary-steps", type=int, default=20)
     ap.add_argument("--extras", action="store_true",
-                    help=f"also time the next-row kernels on the {SECONDARY_CONFIG} table (Muon variants, "
-                         "column-cut RMNP, HTRMNP, graph replay, planner)")
+                    help="also time the next-row kernels (Muon variants, column-cut RMNP, HTRMNP, graph "
+                         "replay, planner) on the --extras-config table")
+    ap.add_argument("--extras-config", default=SECONDARY_CONFIG)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -159,8 +159,10 @@ int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params*
  *  - Tables whose mo_muon_workspace_bytes() exceeds that size are rejected
  *    with MO_ERR_SCRATCH_LIMIT before anything is enqueued.
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress with that device current); make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress with that device current) and keeps it for the
+ *    life of the process; make that first call before any stream capture.
+ *    A cudaDeviceReset recreates the device's context and may move the
+ *    array, so calls after one are not supported.
  *  - All calls share the one array and it keeps the last call's contents;
  *    each call rewrites everything the step needs zeroed. Calls that overlap
  *    on the GPU (different streams, or concurrent host threads) race on it.

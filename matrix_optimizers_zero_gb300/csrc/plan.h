@@ -30,8 +30,8 @@ struct MuonLayout {
   int64_t cast_total = 0;
   size_t off_meta = 0, off_tmaps = 0, off_seg_prefix = 0, off_seg_code = 0, off_counters = 0, off_ready = 0,
          off_abort = 0;
-  size_t off_lr = 0;
-  size_t off_reduces = 0;                 // one fp32: the learning rate a planned step reads (mo_muon_plan)
+  size_t off_lr = 0;                 // one fp32: the learning rate a planned step reads (mo_muon_plan)
+  size_t off_reduces = 0;
   size_t off_tiles[3] = {0, 0, 0};
   size_t header_bytes = 0;           // [0, header_bytes) is uploaded by every call
   size_t off_partials = 0, off_scales = 0, off_buffers = 0;

@@ -36,7 +36,9 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 // Device address of g_static_scratch per device. In host code the array's
 // name is only a host-side stand-in, so the address must come from
-// cudaGetSymbolAddress with the device current.
+// cudaGetSymbolAddress with the device current. It is looked up on the first
+// call on each device and kept for the life of the process (a
+// cudaDeviceReset, after which the array may move, is not supported).
 struct ScratchAddr {
   bool ready = false;
   void* ptr = nullptr;
