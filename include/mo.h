@@ -315,6 +315,24 @@ enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
 int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase,
                           mo_tile* out, int64_t cap, int64_t* count);
 
+/* Test support (no counterpart on the pages): muon_owner_step that also
+ * counts on the device how often each Newton-Schulz output tile was executed.
+ *  - *needed (must not be NULL) receives the number of uint32 counters: two
+ *    per tile (the even and the odd CTA of the pair that computes it) for
+ *    every GEMM launch of the step, in launch order (per iteration: Gram,
+ *    then A.A (appendix form: A.X), then B.X), each launch's tiles in its
+ *    launch order (mo_muon_tile_schedule; a long Gram's slices are separate
+ *    tiles there).
+ *  - coverage NULL: nothing runs (size query, host only). Otherwise
+ *    `coverage` is a caller-zeroed device buffer of coverage_len counters
+ *    (MO_ERR_BAD_SHAPE if fewer than *needed) and the step runs as
+ *    muon_owner_step would, with the same results; every counter reads 1
+ *    afterwards when each tile ran exactly once on each CTA of its pair.
+ * Other arguments and status codes as muon_owner_step. */
+int muon_owner_step_coverage(const mo_matrix* tbl, int32_t n, const mo_muon_params* params,
+                             void* ws, size_t ws_bytes, uint32_t* coverage, int64_t coverage_len,
+                             int64_t* needed, cudaStream_t stream);
+
 /* ---- owner planning ("MatrixFSDP", section 4.1, Algorithm 1) ----
  * A role is one 2D matrix or the packed non-matrix tail of one block. The
  * planner assigns every role whole to one of `world` owner ranks, balancing

@@ -178,10 +178,20 @@ int insert_plan(PlanEntry* e, const mo_matrix* tbl, int32_t n, void* ws, bool wa
 namespace mo {
 
 int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* prm, const float* lr_dev,
-                 DeviceInfo* dev, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end);
+                 DeviceInfo* dev, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end,
+                 uint32_t* coverage);
+
+// Tile-execution counters of one step (muon_owner_step_coverage): two per
+// tile of every Newton-Schulz GEMM launch, launches in order.
+int64_t coverage_counters(const mo::MuonLayout& L, const mo_muon_params* prm) {
+  const int mid = prm->ns_form == MO_NS_APPENDIX ? MO_PHASE_UPDATE : MO_PHASE_POLY;
+  return 2 * int64_t(prm->ns_steps) *
+         int64_t(L.tiles[MO_PHASE_GRAM].size() + L.tiles[mid].size() + L.tiles[MO_PHASE_UPDATE].size());
+}
 
 int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* ws, size_t ws_bytes,
-                   cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end, bool allow_pinned) {
+                   cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end, bool allow_pinned,
+                   uint32_t* coverage, int64_t coverage_len) {
   int st = mo::validate_muon_params(prm);
   if (st != MO_OK) return st;
   if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
@@ -206,6 +216,10 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   if (ws_bytes < need) {
     delete fresh;
     return MO_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (coverage != nullptr && coverage_len < coverage_counters(E ? E->L : fresh->L, prm)) {
+    delete fresh;
+    return MO_ERR_BAD_SHAPE;
   }
   DeviceInfo* dev = nullptr;
   int dev_id = 0;
@@ -239,13 +253,14 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   if (e != cudaSuccess) return cuda_fail(e);
   if (use_pinned && (e = cudaEventRecord(E->uploaded, stream)) != cudaSuccess) return cuda_fail(e);
 
-  return enqueue_muon(L, wsb, prm, nullptr, dev, stream, ev_begin, ev_end);
+  return enqueue_muon(L, wsb, prm, nullptr, dev, stream, ev_begin, ev_end, coverage);
 }
 
 // The prologue and Newton-Schulz launches of one step whose workspace header
 // is in place; the learning rate comes from `lr_dev` when it is set.
 int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* prm, const float* lr_dev,
-                 DeviceInfo* dev, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
+                 DeviceInfo* dev, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end,
+                 uint32_t* coverage) {
   cudaError_t e;
   const mo::DevMat* d_mats = reinterpret_cast<const mo::DevMat*>(wsb + L.off_meta);
   float* d_scales = reinterpret_cast<float*>(wsb + L.off_scales);
@@ -294,6 +309,8 @@ int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* pr
       np.ntiles = int32_t(L.tiles[sched[k]].size());
       const bool last = (k == 2) && (it == prm->ns_steps - 1);
       const int grid = 2 * std::max(1, std::min(np.ntiles, dev->sms / 2));
+      np.coverage = coverage;
+      if (coverage != nullptr) coverage += 2 * size_t(np.ntiles);
       if ((e = mo::launch_ns_phase(kinds[k], last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
       if (k == 0 && L.reduce_blocks > 0) {
         // long matrices: A = sum of the slice partials
@@ -480,7 +497,7 @@ int mo_muon_plan_step(mo_muon_plan plan, cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(plan->ws + L.off_counters, 0, L.off_lr - L.off_counters, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return mo::enqueue_muon(L, plan->ws, &plan->params, reinterpret_cast<const float*>(plan->ws + L.off_lr), dev,
-                          stream, nullptr, nullptr);
+                          stream, nullptr, nullptr, nullptr);
 }
 
 float* mo_muon_plan_lr_ptr(mo_muon_plan plan) {
@@ -503,12 +520,30 @@ size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_pa
 
 int muon_owner_step(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws, size_t ws_bytes,
                     cudaStream_t stream) {
-  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr, true);
+  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr, true, nullptr, 0);
 }
 
 int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws,
                           size_t ws_bytes, cudaStream_t stream, cudaEvent_t ev_ns_begin, cudaEvent_t ev_ns_end) {
-  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, ev_ns_begin, ev_ns_end, true);
+  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, ev_ns_begin, ev_ns_end, true, nullptr, 0);
+}
+
+int muon_owner_step_coverage(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws,
+                             size_t ws_bytes, uint32_t* coverage, int64_t coverage_len, int64_t* needed,
+                             cudaStream_t stream) {
+  if (!needed) return MO_ERR_NULL_POINTER;
+  int st = mo::validate_muon_params(params);
+  if (st != MO_OK) return st;
+  if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
+  if (n == 0) {
+    *needed = 0;
+    return MO_OK;
+  }
+  mo::MuonLayout L;
+  mo::plan_muon(tbl, n, mo::kBM, params->ns_form, L);
+  *needed = mo::coverage_counters(L, params);
+  if (coverage == nullptr) return MO_OK;   // size query
+  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr, true, coverage, coverage_len);
 }
 
 int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cudaStream_t stream) {

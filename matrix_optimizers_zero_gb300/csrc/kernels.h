@@ -24,6 +24,7 @@ struct NsParams {
   const float* lr_dev;        // when set, the learning rate is read from this device float instead of `lr`
   int32_t lr_adjust;          // mo_lr_adjust: which per-matrix scale the update uses
   uint64_t timeout_ns;
+  uint32_t* coverage;         // tests only (null otherwise): per tile, two execution counters (even, odd CTA)
 };
 
 // 256 x 256 tiles on CTA pairs; grid must be even (two CTAs per cluster).

@@ -506,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+      if (p.coverage != nullptr && warp == 2 && lane == 0) atomicAdd(p.coverage + 2 * size_t(t) + rank, 1u);
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }

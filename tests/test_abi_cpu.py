@@ -297,3 +297,24 @@ def test_device_hyperparameter_validation_codes(lib):
     assert lib.rmnp_step_dev(tp, 1, ctypes.byref(mo.RmnpParams()), ctypes.c_float(2.0), lr_ptr, None) == -4
     assert lib.rmnp_step_dev(None, 0, ctypes.byref(mo.RmnpParams(lr=float("nan"))), ctypes.c_float(0.0),
                              lr_ptr, None) == 0
+
+
+def test_tile_coverage_size_query(lib):
+    """muon_owner_step_coverage with no buffer only reports how many counters
+    a step needs: two per tile of every GEMM launch (Gram, A.A or A.X, B.X per
+    iteration), the tile counts being those of the host schedule."""
+    for shapes, form, steps in (([(130, 257), (300, 200), (1, 70_000)], "gram", 5),
+                                ([(1280, 5120)] * 3 + [(64, 1)], "appendix", 2)):
+        p = mo.MuonParams(ns_form=form, ns_steps=steps)
+        arr = mo.fake_table(shapes)
+        need = ctypes.c_int64(-1)
+        st = lib.muon_owner_step_coverage(ctypes.cast(arr, ctypes.c_void_p), len(shapes), ctypes.byref(p), None, 0,
+                                          None, 0, ctypes.byref(need), None)
+        assert st == 0
+        mid = 1 if form == "gram" else 2
+        per_iter = sum(len(mo.mo_muon_tile_schedule(shapes, ph)) for ph in (0, mid, 2))
+        assert need.value == 2 * steps * per_iter
+    # a null count pointer is rejected before anything else
+    arr = mo.fake_table([(16, 32)])
+    assert lib.muon_owner_step_coverage(ctypes.cast(arr, ctypes.c_void_p), 1, ctypes.byref(mo.MuonParams()), None, 0,
+                                        None, 0, None, None) == -1
