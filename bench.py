@@ -44,7 +44,14 @@ UNIT = "TFLOP/s"
 # the table's matrices). Valid only for the kernel source and tile schedule it
 # was measured on (hash of ns_gemm.cu and plan.cpp); the profiles directory
 # holds the capture summaries with their commands.
-NS_TRAFFIC = {}
+NS_TRAFFIC = {
+    "llama8b": {"source_sha256_16": "a11446175fb4bcec", "bytes_per_ns_segment": 963.411e9,
+                "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
+                       "fourth step on the full table"},
+    "gpt2l": {"source_sha256_16": "a11446175fb4bcec", "bytes_per_ns_segment": 37.224e9,
+              "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
+                     "fourth step on the full table"},
+}
 # A timed region at least this long is "a kernel timed inside a long step":
 # its roofline uses the sustained bf16 peak, a shorter one the burst peak.
 SUSTAINED_REGION_S = 1.0
