@@ -589,10 +589,15 @@ def end_to_end(args, mo, owner, dev, stream, barrier, world, ns_flops):
     """The same step through the C ABI with host buffers. Every step uploads
     its gradients (Muon/RMNP G and the tail's g) from pinned host memory and
     reads all updated weights back (Muon W, RMNP W, tail p). Uploads, compute
-    and read-backs run on three streams: the gradients are double-buffered on
-    the device so step k+1's upload overlaps step k; a step's Muon call waits
-    until the previous step's Muon weights have been read back, its AdamW and
-    RMNP calls until the previous RMNP weights and tail have been."""
+    and read-backs run on three streams. The gradients are double-buffered on
+    the device, so step k+1's upload overlaps step k. The weights are updated
+    in place, so each step snapshots them into device staging buffers right
+    after its Muon (W) and RMNP/AdamW (RMNP W, tail p) calls; the read-back
+    copies from the snapshots while the next step computes (a snapshot waits
+    only until the previous step's read-back of that buffer is done). The
+    snapshots are elementwise kernels (x * 1.0, bit-identical), not
+    device-to-device memcpys: those would queue on the copy engines behind
+    the read-backs and stall the compute stream."""
     import torch
     if args.no_e2e:
         return None
@@ -617,6 +622,14 @@ def end_to_end(args, mo, owner, dev, stream, barrier, world, ns_flops):
     hTg.copy_(owner.Tg)
     Gf, Tg = owner.Gf, owner.Tg
     Gf2, Tg2 = torch.empty_like(Gf), torch.empty_like(Tg)
+    try:
+        sW, sWr, sP = torch.empty_like(owner.Wf), torch.empty_like(owner.Wr), torch.empty_like(owner.Pf)
+        staged = True
+    except torch.cuda.OutOfMemoryError:
+        # no room for the snapshots: read back from the live weights, each
+        # step waiting until the previous read-back of them is done
+        sW, sWr, sP = owner.Wf, owner.Wr, owner.Pf
+        staged = False
     mo_ = owner.mo
     bufs = [(Gf, Tg, (owner.muon_tbl, owner.rmnp_tbl, owner.tail_tbl)),
             (Gf2, Tg2, (mo_.MuonTable(list(zip(owner.W_l, owner.views(Gf2), owner.V_l))),
@@ -642,25 +655,35 @@ def end_to_end(args, mo, owner, dev, stream, barrier, world, ns_flops):
             Tgd.copy_(hTg, non_blocking=True)
         ev_in[b].record(s_in)
         stream.wait_event(ev_in[b])
-        if k >= 1:
-            stream.wait_event(ev_wout)
+
+        if k >= 1 and not staged:
+            stream.wait_event(ev_wout)        # W is read back from the live buffer
 
         def after_muon():
+            if staged:
+                if k >= 1:
+                    stream.wait_event(ev_wout)    # the previous snapshot of W has been read back
+                torch.mul(owner.Wf, 1.0, out=sW)
             ev_w.record(stream)
-            if k >= 1:
+            if k >= 1 and not staged:
                 stream.wait_event(ev_rout)
 
         owner.step(stream, tabs=tabs, between=after_muon)
-        ev_r.record(stream)
         ev_free[b].record(stream)
+        if staged:
+            if k >= 1:
+                stream.wait_event(ev_rout)
+            torch.mul(owner.Wr, 1.0, out=sWr)
+            torch.mul(owner.Pf, 1.0, out=sP)
+        ev_r.record(stream)
         s_out.wait_event(ev_w)
         with torch.cuda.stream(s_out):
-            hW.copy_(owner.Wf, non_blocking=True)
+            hW.copy_(sW, non_blocking=True)
         ev_wout.record(s_out)
         s_out.wait_event(ev_r)
         with torch.cuda.stream(s_out):
-            hWr.copy_(owner.Wr, non_blocking=True)
-            hP.copy_(owner.Pf, non_blocking=True)
+            hWr.copy_(sWr, non_blocking=True)
+            hP.copy_(sP, non_blocking=True)
         ev_rout.record(s_out)
     stream.wait_event(ev_rout)
     e1.record(stream)
@@ -683,7 +706,10 @@ def end_to_end(args, mo, owner, dev, stream, barrier, world, ns_flops):
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms_max, 3), "steps": e2e_steps,
             "link_measured": link, "pinned_alloc_s": round(pin_s, 1),
             "copies": "pinned host buffers; uploads, compute and read-backs on three streams, "
-                      "gradients double-buffered on the device"}
+                      "gradients double-buffered on the device, "
+                      + ("updated weights snapshotted on the device (an elementwise copy kernel inside the "
+                         "step) and read back from the snapshots" if staged else
+                         "updated weights read back from the live buffers (no device memory for snapshots)")}
 
 
 # ---------------------------------------------------------------- next-row kernels (--extras)
