@@ -132,6 +132,12 @@ def get_workload(name: str) -> Workload:
     if name == "llama8b":
         m, t = _llama8b()
         return Workload("llama8b", 2, m, t, w_std=0.02, g_std=1e-3, tail_p_std=0.02, tail_g_std=1e-3)
+    if name == "gram_slices":
+        # one 4096 x 40000 matrix: its Gram (n = 40000 > 32768) is summed from
+        # two fp32 slice partials (2 x 64 MB, larger than L2); used to profile
+        # the slice reduction
+        return Workload("gram_slices", 7, (MatrixSpec(4096, 40000, "long"),), (4096,), w_std=0.02, g_std=1e-3,
+                        tail_p_std=0.02, tail_g_std=1e-3)
     if name == "llama8b_1layer":
         # one layer of the Llama-style 8B set (7 matrices, 218 M elements) and a
         # tail of its two RMSNorm vectors plus one eighth of the embedding
