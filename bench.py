@@ -112,6 +112,11 @@ def max_over_ranks(x: float, device=None) -> float:
     return float(t.item())
 
 
+def min_over_ranks(x: float, device=None) -> float:
+    """The minimum of x over all ranks (x itself without a process group)."""
+    return -max_over_ranks(-float(x), device)
+
+
 def whole_job_tflops(world: int, flops_per_rank: float, ms_max: float) -> float:
     """Aggregate throughput of `world` independent replicas that each did
     flops_per_rank of work, timed by the slowest rank."""
@@ -603,10 +608,16 @@ def end_to_end(args, mo, owner, dev, stream, barrier, world, ns_flops):
         return None
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     need = owner.Gf.numel() * 2 + owner.Tg.numel() * 4 + (owner.Wf.numel() + owner.Wr.numel() + owner.Pf.numel()) * 4
+    # the ranks of one host share its memory; every rank takes the same
+    # decision (the leg has barriers)
+    local_world = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
     avail = host_mem_available_bytes()
-    if avail is not None and need > 0.7 * avail:
+    fits = avail is None or need <= 0.7 * avail / local_world
+    if not (min_over_ranks(1.0 if fits else 0.0, dev) > 0.0):
+        share = (avail or 0) / local_world
         return {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
-                "unavailable": f"pinned host buffers need {need / 1e9:.1f} GB, host has {avail / 1e9:.1f} GB available"}
+                "unavailable": f"pinned host buffers need {need / 1e9:.1f} GB per rank, a rank's share of the host's "
+                               f"available memory is {share / 1e9:.1f} GB"}
     t_pin = time.perf_counter()
     hG = torch.empty(owner.Gf.numel(), dtype=torch.bfloat16, pin_memory=True)
     hTg = torch.empty(owner.Tg.numel(), dtype=torch.float32, pin_memory=True)

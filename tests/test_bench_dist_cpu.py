@@ -27,11 +27,14 @@ def _worker(rank, world, port, out):
     local_ms = 10.0 + 5.0 * rank                 # rank 1 is the slowest replica
     ms_max = bench.max_over_ranks(local_ms)
     value = bench.whole_job_tflops(world, 2e12, ms_max)
+    # a decision every rank must share (the end-to-end leg's memory check):
+    # one rank without room makes all of them skip
+    agreed = bench.min_over_ranks(1.0 if rank == 0 else 0.0)
 
     class Args:
         config, steps, warmup = "smoke", 1, 3
     ref = bench.run_reference(Args(), rank)
-    out[rank] = (ms_max, value, ref is None)
+    out[rank] = (ms_max, value, ref is None, agreed)
     dist.barrier()
     dist.destroy_process_group()
 
@@ -41,8 +44,9 @@ def test_two_rank_replicas_gloo():
     out = mp.Manager().dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     for rank in range(world):
-        ms_max, value, ref_none = out[rank]
+        ms_max, value, ref_none, agreed = out[rank]
         assert ms_max == 15.0
+        assert agreed == 0.0
         assert value == pytest.approx(2 * 2e12 / 15e-3 / 1e12)
         assert ref_none == (rank != 0)
 
@@ -51,4 +55,5 @@ def test_single_process_helpers():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.min_over_ranks(2.5) == 2.5
     assert bench.whole_job_tflops(1, 1e12, 1000.0) == pytest.approx(1.0)
