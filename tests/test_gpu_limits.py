@@ -1,5 +1,9 @@
 """The largest supported sizes, against the oracle.
 
+* Muon at the largest supported short side (65536 x 65536): a sign-pattern
+  gradient that keeps every stored value exact, checked element for element
+  against the oracle's scalar recursion (see the test).
+
 * Muon and RMNP on matrices at the longest supported dimension (2^22 columns
   or rows; 16384 tile columns of 256) with one to three rows, ragged in both
   directions: full comparison, since such matrices are cheap for the oracle.
@@ -99,3 +103,48 @@ def test_adamw_segment_beyond_2_31_elements():
         assert max_rel(f64(got[it]), want) <= FP32_MAX_REL_TOL
     del pt, g, m, v
     torch.cuda.empty_cache()
+
+
+def test_muon_largest_square_sign_matrix():
+    """m = n = 65536, the largest supported short side: the Gram is split
+    into two slices, and A.A and B.X reduce over 65536 unsplit. The gradient
+    is an outer product of random +-1 vectors times 2^-10, so every value the
+    iteration stores is an exact power-of-two multiple of the same sign
+    pattern: X_k = x_k s t^T / sqrt(m n), A_k = x_k^2 s s^T / m, and every
+    fp32 sum of the products is exact. The iteration is then a scalar
+    recursion whose bf16 roundings depend only on mantissas, so the oracle
+    on a 64 x 64 matrix of the same kind gives the value the 65536 x 65536
+    result must have. Checks: the momentum equals G exactly; every element of
+    the update is the same value up to its sign s_i t_j (bit for bit: any
+    tile computed wrongly, twice or not at all would break this); and that
+    value matches the oracle's within the Newton-Schulz tolerance."""
+    m = 65536
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(11)
+    s = torch.randint(0, 2, (m,), generator=gen, device=DEV).float().mul_(2).sub_(1)
+    t = torch.randint(0, 2, (m,), generator=gen, device=DEV).float().mul_(2).sub_(1)
+    G = torch.empty(m, m, device=DEV, dtype=torch.bfloat16)
+    for r0 in range(0, m, 4096):
+        G[r0:r0 + 4096] = (s[r0:r0 + 4096, None] * t[None, :] * 2.0 ** -10).to(torch.bfloat16)
+    W = torch.zeros(m, m, device=DEV)
+    V = torch.zeros(m, m, device=DEV)
+    p = mo.MuonParams(lr=1.0, wd=0.0)
+    ws = mo.muon_workspace([(W, G, V)], p, device=DEV)
+    mo.muon_owner_step([(W, G, V)], p, ws)
+    torch.cuda.synchronize()
+    assert mo.mo_last_device_error() == 0
+    del ws
+    # the oracle's value of x_5 on a small matrix of the same structure
+    rs = np.random.default_rng(0)
+    ss, tt = rs.choice([-1.0, 1.0], 64), rs.choice([-1.0, 1.0], 64)
+    _, _, O = oracle.muon_matrix_step(np.zeros((64, 64)), np.outer(ss, tt) * 2.0 ** -10, np.zeros((64, 64)),
+                                      **oracle_options(p))
+    x5 = float((O * np.outer(ss, tt)).ravel()[0] * 64)
+    lo, hi = float("inf"), -float("inf")
+    for r0 in range(0, m, 4096):
+        rows = slice(r0, r0 + 4096)
+        assert torch.equal(V[rows], G[rows].float())
+        d = W[rows] * s[rows, None] * t[None, :] * (-float(m))   # exact: powers of two and signs
+        lo, hi = min(lo, float(d.min())), max(hi, float(d.max()))
+    assert lo == hi, (lo, hi)
+    assert abs(lo - x5) <= NS_REL_FROB_TOL * abs(x5), (lo, x5)
