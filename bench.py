@@ -307,15 +307,15 @@ class Owner:
                                   for o, t in zip(self.toffs, self.tail_sizes)])
 
     def launches_per_step(self):
-        """Kernel launches of one step: the prologue, 3 GEMM launches per
-        iteration (plus one Gram reduction per iteration when a matrix has
+        """Kernel launches of one step: the prologue (a norm and a cast
+        launch), 3 GEMM launches per iteration (plus one Gram reduction per iteration when a matrix has
         more than 32768 columns on its long side), AdamW one per 256 segments,
         RMNP one per 512 entries separately for rows shorter / not shorter
         than 8192 elements."""
         wl = self.wl
         n_long = sum(1 for _, c in self.shapes if c >= 8192)
         reduce = 1 if any(max(r, c) > 32768 for r, c in self.shapes) else 0
-        return ((1 + (3 + reduce) * wl.ns_steps) + math.ceil(len(self.tail_sizes) / 256)
+        return ((2 + (3 + reduce) * wl.ns_steps) + math.ceil(len(self.tail_sizes) / 256)
                 + math.ceil((len(self.shapes) - n_long) / 512) + math.ceil(n_long / 512))
 
     def step(self, stream, ev=None, tabs=None, between=None):

@@ -122,8 +122,8 @@ int bind_header(mo::MuonLayout& L, void* ws, std::vector<uint8_t>& header) {
   if (!L.reduces.empty())
     std::memcpy(header.data() + L.off_reduces, L.reduces.data(), sizeof(mo::GramReduce) * L.reduces.size());
   std::memcpy(header.data() + L.off_meta, L.mats.data(), sizeof(mo::DevMat) * L.mats.size());
-  std::memcpy(header.data() + L.off_seg_prefix, L.seg_prefix.data(), sizeof(int64_t) * L.seg_prefix.size());
-  std::memcpy(header.data() + L.off_seg_code, L.seg_code.data(), sizeof(int32_t) * L.seg_code.size());
+  std::memcpy(header.data() + L.off_nrm_prefix, L.nrm_prefix.data(), sizeof(int64_t) * L.nrm_prefix.size());
+  std::memcpy(header.data() + L.off_cast_prefix, L.cast_prefix.data(), sizeof(int64_t) * L.cast_prefix.size());
   for (int ph = 0; ph < 3; ++ph)
     if (!L.tiles[ph].empty())
       std::memcpy(header.data() + L.off_tiles[ph], L.tiles[ph].data(), sizeof(mo::TileRec) * L.tiles[ph].size());
@@ -237,7 +237,6 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   }
   if (E == nullptr) {
     fresh->dev = dev_id;
-    mo::order_prologue(fresh->L, int64_t(mo::kPrologueCtasPerSm) * dev->sms);
     if ((st = insert_plan(fresh, tbl, n, ws, allow_pinned)) != MO_OK) {
       delete fresh;
       return st;
@@ -267,16 +266,17 @@ int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* pr
 
   mo::ProParams pp{};
   pp.mats = d_mats;
-  pp.seg_prefix = reinterpret_cast<const int64_t*>(wsb + L.off_seg_prefix);
-  pp.seg_code = reinterpret_cast<const int32_t*>(wsb + L.off_seg_code);
+  pp.nrm_prefix = reinterpret_cast<const int64_t*>(wsb + L.off_nrm_prefix);
+  pp.cast_prefix = reinterpret_cast<const int64_t*>(wsb + L.off_cast_prefix);
   pp.partials = reinterpret_cast<float*>(wsb + L.off_partials);
   pp.counters = reinterpret_cast<uint32_t*>(wsb + L.off_counters);
   pp.ready = reinterpret_cast<uint32_t*>(wsb + L.off_ready);
   pp.abort = reinterpret_cast<uint32_t*>(wsb + L.off_abort);
   pp.scales = d_scales;
   pp.status = dev->status;
-  pp.nseg = int32_t(L.seg_code.size());
-  pp.total_items = L.seg_prefix.back();
+  pp.n = L.n;
+  pp.nrm_total = L.nrm_prefix.back();
+  pp.cast_total = L.cast_prefix.back();
   pp.mu = prm->mu;
   pp.eps = prm->eps;
   pp.nesterov = prm->nesterov;
@@ -465,7 +465,6 @@ int mo_muon_plan_create(const mo_matrix* tbl, int32_t n, const mo_muon_params* p
     delete P;
     return st != MO_OK ? st : cuda_fail(cudaErrorInvalidDevice);
   }
-  mo::order_prologue(P->L, int64_t(mo::kPrologueCtasPerSm) * dev->sms);
   std::vector<uint8_t> header;
   if ((st = bind_header(P->L, ws, header)) != MO_OK) {
     delete P;

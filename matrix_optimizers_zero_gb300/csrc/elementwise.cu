@@ -23,33 +23,35 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // ------------------------------------------------------------------ Muon prologue
 //
-// One persistent cooperative launch over a work list of two item kinds:
-//   norm items   momentum V <- mu V + G ("Optimizers In A Sharded World",
-//                section 1) over a flat 32768-element chunk of a stored
-//                matrix, with one fp32 sum of squares of U per chunk, where
-//                U = V, or U = G + mu V with Nesterov momentum (the default
-//                update of torch.optim.Muon, which "MatrixFSDP" section 5.1
-//                runs). The CTA that completes a matrix's last chunk sums
-//                that matrix's partials in a fixed order (deterministic, no
-//                float atomics), writes the Frobenius scale 1 / (||U|| + eps)
-//                (eps added to the norm, as in the same page's appendix) and
-//                marks the matrix ready.
-//   cast items   X0 = bf16(U * scale) for a 64 x 128 tile, written in the wide
+// Two launches over the owner's table:
+//   norm launch  momentum V <- mu V + G ("Optimizers In A Sharded World",
+//                section 1) over flat kNrmChunk-element chunks of every
+//                stored matrix, with one fp32 sum of squares of U per chunk,
+//                where U = V, or U = G + mu V with Nesterov momentum (the
+//                default update of torch.optim.Muon, which "MatrixFSDP"
+//                section 5.1 runs). The CTA that completes a matrix's last
+//                chunk sums that matrix's partials in a fixed order
+//                (deterministic, no float atomics) and writes the Frobenius
+//                scale 1 / (||U|| + eps) (eps added to the norm, as in the
+//                same page's appendix).
+//   cast launch  X0 = bf16(U * scale) for 64 x 128 tiles, written in the wide
 //                orientation (transposed through shared memory when
-//                rows > cols, appendix of the same page).
-// The list interleaves matrices (norm 0, norm 1, cast 0, norm 2, cast 1, ...)
-// so a matrix is cast while its fresh momentum is still in L2. A cast item
-// waits (bounded) for its matrix to be ready; every dependency points to an
-// earlier item, and all CTAs are co-resident, so the waits always end.
+//                rows > cols, appendix of the same page). It is a
+//                programmatic dependent launch that waits for the norm
+//                launch to complete, so every scale is final and nothing
+//                waits inside it; tiles are taken from the last matrix back,
+//                last row block first, so the momentum the norm launch wrote
+//                last is read while it is still in L2.
+// Both are grid-stride streams with many 16-byte loads in flight per thread
+// (the norm launch 16 vectors of V and 16 of G, at two CTAs per SM), which is
+// what a memory-bound kernel needs here to keep HBM busy. (A single launch
+// that interleaves the casts with the norms, to re-read the momentum from L2,
+// moves fewer bytes but has to make casts wait for their matrix's norm.)
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
-// 16-byte vectors per thread loaded before use in each round of a norm item
-constexpr int kNrmBatch = 4;
+// 16-byte vectors of V (and the matching 8 bytes of G) per thread loaded
+// before use in each round of a norm item
+constexpr int kNrmBatch = 16;
 
 template <bool NEST>
 __device__ void prologue_norm_item(const ProParams& p, int mi, int64_t local, float* red, int* last_flag) {
@@ -140,31 +142,6 @@ __device__ void prologue_norm_item(const ProParams& p, int mi, int64_t local, fl
   __syncthreads();
 }
 
-// Thread 0 waits for the matrix's scale; returns false (for the whole CTA)
-// if the wait gave up or another CTA of the launch already gave up.
-__device__ bool prologue_wait_ready(const ProParams& p, int mi, int* ok_flag) {
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    if (ld_acquire(&p.ready[mi]) == 0u) {
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (true) {
-        if (ld_acquire(&p.ready[mi]) != 0u) break;
-        if (ld_acquire(p.abort) != 0u) { ok = 0; break; }
-        if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
-          atomicExch(p.abort, 1u);
-          atomicExch(p.status, MO_ERR_DEVICE_TIMEOUT);
-          ok = 0;
-          break;
-        }
-        __nanosleep(128);
-      }
-    }
-    *ok_flag = ok;
-  }
-  __syncthreads();
-  return *ok_flag != 0;
-}
-
 // U = V, or G + mu V (Nesterov), for four consecutive elements at `off`.
 template <bool NEST>
 __device__ __forceinline__ float4 load_u4(const ProParams& p, const DevMat& M, size_t off) {
@@ -197,22 +174,21 @@ __device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, ui
   const size_t ldx = size_t(M.ldx);
   if (!M.tall) {
     // warp w covers rows w, w+8, ...; lanes cover 4 consecutive columns each.
-    // Rows go in batches of four whose loads are all issued before the
-    // batch's stores (the stores could alias the loads as far as the
+    // All eight rows' loads are issued before their stores (the stores could alias the loads as far as the
     // compiler knows, which would otherwise serialise every row on a full
     // memory latency).
     const int c = c0 + lane * 4;
     if (c < C && M.vec_ok && c + 4 <= C) {
 #pragma unroll 1
-      for (int i0 = 0; i0 < kCastTR / 8; i0 += 4) {
-        float4 u[4];
+      for (int i0 = 0; i0 < kCastTR / 8; i0 += 8) {
+        float4 u[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const int r = r0 + warp + 8 * (i0 + i);
           if (r < R) u[i] = load_u4<NEST>(p, M, size_t(r) * size_t(C) + size_t(c));
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const int r = r0 + warp + 8 * (i0 + i);
           if (r < R)
             *reinterpret_cast<uint2*>(X + size_t(r) * ldx + size_t(c)) =
@@ -289,27 +265,36 @@ __device__ void prologue_cast_item(const ProParams& p, int mi, int64_t local, ui
   }
 }
 
+// Index of the matrix whose prefix range [prefix[i], prefix[i+1]) holds t.
+__device__ __forceinline__ int prologue_matrix(const int64_t* prefix, int n, int64_t t) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 template <bool NEST>
-__global__ void __launch_bounds__(256, kPrologueCtasPerSm) muon_prologue_kernel(const __grid_constant__ ProParams p) {
-  ptx::griddep_launch_dependents();   // the first Gram launch may start its setup as CTAs finish
-  __shared__ __align__(16) uint16_t tbuf[kCastTC][kCastTR + 8];
+__global__ void __launch_bounds__(256, kPrologueCtasPerSm) muon_norm_kernel(const __grid_constant__ ProParams p) {
+  ptx::griddep_launch_dependents();   // the cast launch is scheduled early; it waits for this grid to finish
   __shared__ float red[8];
   __shared__ int flag;
-  for (int64_t t = blockIdx.x; t < p.total_items; t += gridDim.x) {
-    int lo = 0, hi = p.nseg - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.seg_prefix[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    const int code = p.seg_code[lo];
-    const int mi = code >> 1;
-    const int64_t local = t - p.seg_prefix[lo];
-    if ((code & 1) == 0) {
-      prologue_norm_item<NEST>(p, mi, local, red, &flag);
-    } else {
-      if (!prologue_wait_ready(p, mi, &flag)) return;   // uniform across the CTA
-      prologue_cast_item<NEST>(p, mi, local, tbuf);
-    }
+  for (int64_t t = blockIdx.x; t < p.nrm_total; t += gridDim.x) {
+    const int mi = prologue_matrix(p.nrm_prefix, p.n, t);
+    prologue_norm_item<NEST>(p, mi, t - p.nrm_prefix[mi], red, &flag);
+  }
+}
+
+template <bool NEST>
+__global__ void __launch_bounds__(256) muon_cast_kernel(const __grid_constant__ ProParams p) {
+  __shared__ __align__(16) uint16_t tbuf[kCastTC][kCastTR + 8];
+  ptx::griddep_wait();                // the norm launch's momentum and scales
+  ptx::griddep_launch_dependents();   // the first Gram launch may start its setup as CTAs finish
+  for (int64_t t = blockIdx.x; t < p.cast_total; t += gridDim.x) {
+    const int64_t r = p.cast_total - 1 - t;   // from the last tile of the last matrix back
+    const int mi = prologue_matrix(p.cast_prefix, p.n, r);
+    prologue_cast_item<NEST>(p, mi, r - p.cast_prefix[mi], tbuf);
   }
 }
 
@@ -739,20 +724,37 @@ __global__ void __launch_bounds__(256) adamw_kernel(const __grid_constant__ Adam
 }  // namespace
 
 cudaError_t launch_muon_prologue(const ProParams& p, int max_grid, cudaStream_t stream) {
-  if (p.total_items <= 0) return cudaSuccess;
+  if (p.nrm_total <= 0) return cudaSuccess;
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const void* kern = p.nesterov ? reinterpret_cast<const void*>(muon_prologue_kernel<true>)
-                                : reinterpret_cast<const void*>(muon_prologue_kernel<false>);
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0)) != cudaSuccess) return e;
-  int64_t grid = int64_t(sms) * int64_t(per_sm);
+  const void* norm = p.nesterov ? reinterpret_cast<const void*>(muon_norm_kernel<true>)
+                                : reinterpret_cast<const void*>(muon_norm_kernel<false>);
+  const void* cast = p.nesterov ? reinterpret_cast<const void*>(muon_cast_kernel<true>)
+                                : reinterpret_cast<const void*>(muon_cast_kernel<false>);
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm, 256, 0)) != cudaSuccess) return e;
+  int64_t grid = int64_t(sms) * int64_t(std::max(per_sm, 1));
   if (max_grid > 0) grid = std::min<int64_t>(grid, max_grid);
-  grid = std::max<int64_t>(1, std::min<int64_t>(grid, p.total_items));
+  grid = std::max<int64_t>(1, std::min<int64_t>(grid, p.nrm_total));
   ProParams copy = p;
   void* args[] = {&copy};
-  return cudaLaunchCooperativeKernel(kern, dim3(unsigned(grid)), dim3(256), args, 0, stream);
+  if ((e = cudaLaunchKernel(norm, dim3(unsigned(grid)), dim3(256), args, 0, stream)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cast, 256, 0)) != cudaSuccess) return e;
+  int64_t cgrid = int64_t(sms) * int64_t(std::max(per_sm, 1));
+  if (max_grid > 0) cgrid = std::min<int64_t>(cgrid, max_grid);
+  cgrid = std::max<int64_t>(1, std::min<int64_t>(cgrid, p.cast_total));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(cgrid), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, cast, args);
 }
 
 cudaError_t launch_rmnp(const RmnpParams& p, bool row_per_cta, int grid, cudaStream_t stream) {

@@ -43,22 +43,22 @@ cudaError_t launch_bounded_wait_selftest(int* status, uint64_t timeout_ns, cudaS
 // ---------------------------------------------------------------- Muon prologue
 struct ProParams {
   const DevMat* mats;
-  const int64_t* seg_prefix;  // 2n + 1 prefix sums of the work-list segments
-  const int32_t* seg_code;    // 2n segment codes: matrix * 2 + kind
+  const int64_t* nrm_prefix;  // n + 1 prefix sums of the matrices' norm chunks
+  const int64_t* cast_prefix; // n + 1 prefix sums of the matrices' cast tiles
   float* partials;            // one sum of squares per chunk
   uint32_t* counters;         // per matrix, zero on entry, zero again on exit
   uint32_t* ready;            // per matrix, set once its scale is final (zero on entry)
-  uint32_t* abort;            // set when any wait of the launch expired (zero on entry)
+  uint32_t* abort;            // unused by the prologue (zero on entry)
   float* scales;              // 1 / (||U||_F + eps), U = V_new or G + mu V_new
   int* status;                // device status word
-  int32_t nseg;
-  int64_t total_items;
+  int32_t n;
+  int64_t nrm_total, cast_total;
   float mu, eps;
   int32_t nesterov;           // orthogonalise G + mu V_new instead of V_new
   uint64_t timeout_ns;
 };
-// Cooperative launch (all CTAs co-resident): normalise/cast items wait for
-// their matrix's norm, which only depends on earlier items of the list.
+// Two launches: the momentum/norm chunks, then (programmatic dependent
+// launch) the normalise/cast tiles, whose scales are final by then.
 cudaError_t launch_muon_prologue(const ProParams& p, int max_grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- RMNP

@@ -20,7 +20,7 @@ constexpr int kBK = 64;
 // row-major stored matrix; cast items (normalise + bf16 cast, transposed for tall
 // matrices): 64 x 128 tiles of the stored matrix.
 constexpr int64_t kNrmChunk = 32768;
-constexpr int kPrologueCtasPerSm = 4;   // launch bound of the prologue kernel
+constexpr int kPrologueCtasPerSm = 2;   // launch bound of the prologue's norm kernel
 constexpr int kCastTR = 64;
 constexpr int kCastTC = 128;
 

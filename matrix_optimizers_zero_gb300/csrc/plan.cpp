@@ -200,34 +200,6 @@ void build_gram_tiles(const mo_matrix* tbl, int32_t n, int bm, std::vector<TileR
   for (size_t j = 0; j < keys.size(); ++j) out[j] = keys[j].t;
 }
 
-void order_prologue(MuonLayout& L, int64_t window) {
-  // Norm segments in table order; the cast segment of matrix i follows once
-  // `window` items (about one wave of the launch) have been listed after the
-  // last norm chunk of matrix i, so that its casts rarely wait for that norm.
-  const int32_t n = L.n;
-  L.seg_code.clear();
-  std::vector<std::pair<int32_t, int64_t>> due;   // (matrix, listed items at which its casts may start)
-  size_t head = 0;
-  int64_t listed = 0;
-  for (int32_t i = 0; i < n; ++i) {
-    L.seg_code.push_back(2 * i);
-    listed += L.nrm_items[size_t(i)];
-    due.push_back({i, listed + window});
-    while (head < due.size() && due[head].second <= listed) {
-      L.seg_code.push_back(2 * due[head].first + 1);
-      listed += L.cast_items[size_t(due[head].first)];
-      ++head;
-    }
-  }
-  for (; head < due.size(); ++head) L.seg_code.push_back(2 * due[head].first + 1);
-  L.seg_prefix.assign(L.seg_code.size() + 1, 0);
-  for (size_t k = 0; k < L.seg_code.size(); ++k) {
-    const int32_t mat = L.seg_code[k] >> 1;
-    L.seg_prefix[k + 1] =
-        L.seg_prefix[k] + ((L.seg_code[k] & 1) ? L.cast_items[size_t(mat)] : L.nrm_items[size_t(mat)]);
-  }
-}
-
 void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout& L) {
   L.n = n;
   L.ns_form = ns_form;
@@ -262,7 +234,12 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout&
   L.cast_total = cast;
   L.nrm_items = chunks;
   L.cast_items = casts;
-  order_prologue(L, int64_t(kPrologueCtasPerSm) * 152);
+  L.nrm_prefix.assign(size_t(n) + 1, 0);
+  L.cast_prefix.assign(size_t(n) + 1, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    L.nrm_prefix[size_t(i) + 1] = L.nrm_prefix[size_t(i)] + chunks[size_t(i)];
+    L.cast_prefix[size_t(i) + 1] = L.cast_prefix[size_t(i)] + casts[size_t(i)];
+  }
   build_gram_tiles(tbl, n, bm, L.tiles[MO_PHASE_GRAM]);
   build_tiles(tbl, n, MO_PHASE_POLY, bm, L.tiles[MO_PHASE_POLY]);
   build_tiles(tbl, n, MO_PHASE_UPDATE, bm, L.tiles[MO_PHASE_UPDATE]);
@@ -283,10 +260,10 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout&
   off = align_up(off + sizeof(DevMat) * nall, 128);
   L.off_tmaps = off;
   off = align_up(off + kTensorMapBytes * kMapsPerMat * nall, 256);
-  L.off_seg_prefix = off;
-  off = align_up(off + sizeof(int64_t) * L.seg_prefix.size(), 256);
-  L.off_seg_code = off;
-  off = align_up(off + sizeof(int32_t) * L.seg_code.size(), 256);
+  L.off_nrm_prefix = off;
+  off = align_up(off + sizeof(int64_t) * L.nrm_prefix.size(), 256);
+  L.off_cast_prefix = off;
+  off = align_up(off + sizeof(int64_t) * L.cast_prefix.size(), 256);
   L.off_counters = off;
   off = align_up(off + sizeof(uint32_t) * size_t(n), 256);
   L.off_ready = off;

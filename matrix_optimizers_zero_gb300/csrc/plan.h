@@ -15,20 +15,17 @@ struct MuonLayout {
   int32_t n = 0;                     // matrices of the table; mats[n..] are Gram slice entries
   int32_t ns_form = MO_NS_GRAM;
   std::vector<DevMat> mats;          // buffer pointers hold workspace OFFSETS until bound
-  // Prologue work list: 2n segments, the momentum/norm chunks of every
-  // matrix in table order, with the normalise/cast tiles of matrix i placed
-  // about one wave of the launch after its last chunk (order_prologue), so a
-  // matrix is cast soon after its norm is final (while its momentum is still
-  // in L2) but rarely has to wait for it.
-  std::vector<int64_t> seg_prefix;   // 2n + 1 prefix sums of segment sizes
-  std::vector<int32_t> seg_code;     // 2n codes: matrix * 2 + (0 = norm chunks, 1 = cast tiles)
-  std::vector<int64_t> nrm_items, cast_items;   // per matrix
+  // Prologue work: the momentum/norm chunks of every matrix, in table order,
+  // for the norm launch; the normalise/cast tiles for the cast launch (which
+  // takes them from the last matrix back). Prefix sums over the matrices.
+  std::vector<int64_t> nrm_prefix, cast_prefix;   // n + 1
+  std::vector<int64_t> nrm_items, cast_items;     // per matrix
   std::vector<TileRec> tiles[3];     // per phase, launch order (Gram tiles may name slice entries)
   std::vector<GramReduce> reduces;   // long matrices (pointer fields hold offsets until bound)
   int64_t reduce_blocks = 0;         // 64 x 64 upper blocks over all long matrices
   int64_t nrm_total = 0;
   int64_t cast_total = 0;
-  size_t off_meta = 0, off_tmaps = 0, off_seg_prefix = 0, off_seg_code = 0, off_counters = 0, off_ready = 0,
+  size_t off_meta = 0, off_tmaps = 0, off_nrm_prefix = 0, off_cast_prefix = 0, off_counters = 0, off_ready = 0,
          off_abort = 0;
   size_t off_lr = 0;                 // one fp32: the learning rate a planned step reads (mo_muon_plan)
   size_t off_reduces = 0;
@@ -62,10 +59,6 @@ std::vector<GramEntry> gram_slices(const mo_matrix* tbl, int32_t n);
 
 // Gram tile schedule over the entries above (TileRec::mat = entry index).
 void build_gram_tiles(const mo_matrix* tbl, int32_t n, int bm, std::vector<TileRec>& out);
-
-// (Re)orders the prologue work list for a launch that processes about
-// `window` items at a time (CTAs in flight); plan_muon uses 4 x 152.
-void order_prologue(MuonLayout& L, int64_t window);
 
 // Layout of the Muon workspace for a validated table; ns_form (mo_ns_form)
 // sets the size of the B buffers (m x m, or m x n for the appendix form).
