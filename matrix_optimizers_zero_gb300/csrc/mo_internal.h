@@ -19,7 +19,7 @@ constexpr int kBK = 64;
 // Muon prologue norm items (momentum + sum of squares): flat chunks of the
 // row-major stored matrix; cast items (normalise + bf16 cast, transposed for tall
 // matrices): 64 x 128 tiles of the stored matrix.
-constexpr int64_t kNrmChunk = 32768;
+constexpr int64_t kNrmChunk = 131072;
 constexpr int kPrologueCtasPerSm = 2;   // launch bound of the prologue's norm kernel
 constexpr int kCastTR = 64;
 constexpr int kCastTC = 128;
