@@ -45,11 +45,10 @@ UNIT = "TFLOP/s"
 # was measured on (hash of ns_gemm.cu and plan.cpp); the profiles directory
 # holds the capture summaries with their commands.
 NS_TRAFFIC = {
-    "llama8b": {"source_sha256_16": "0cc49228239e7ea2", "bytes_per_ns_segment": 1142.535e9,
+    "llama8b": {"source_sha256_16": "de604d48909ee40b", "bytes_per_ns_segment": 483.992e9,
                 "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
-                       "fourth step on the full table (an earlier capture of the same kernels: 963.4 GB; the L2 "
-                       "re-reads vary from run to run)"},
-    "gpt2l": {"source_sha256_16": "0cc49228239e7ea2", "bytes_per_ns_segment": 37.796e9,
+                       "fourth step on the full table"},
+    "gpt2l": {"source_sha256_16": "de604d48909ee40b", "bytes_per_ns_segment": 34.914e9,
               "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
                      "fourth step on the full table"},
 }

@@ -301,7 +301,8 @@ typedef struct {
 enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
 
 /* Writes the tile schedule of one phase (in launch order) into out[0..cap)
- * and the tile count into *count. Returns MO_OK, or MO_ERR_BAD_SHAPE if cap is
+ * and the tile count into *count. The CTA pairs of a launch take the tiles in
+ * this order from one device counter, each pair the next tile as it frees up. Returns MO_OK, or MO_ERR_BAD_SHAPE if cap is
  * too small (then *count holds the required size). Tiles are sorted by
  * decreasing reduction length K (n for the Gram, m otherwise), ties broken by
  * table index, then tile row and tile column (Gram, A.A) or tile column and

@@ -311,6 +311,7 @@ int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* pr
       const int grid = 2 * std::max(1, std::min(np.ntiles, dev->sms / 2));
       np.coverage = coverage;
       if (coverage != nullptr) coverage += 2 * size_t(np.ntiles);
+      np.tile_ctr = reinterpret_cast<uint32_t*>(wsb + L.off_tile_ctr) + (3 * it + k);
       if ((e = mo::launch_ns_phase(kinds[k], last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
       if (k == 0 && L.reduce_blocks > 0) {
         // long matrices: A = sum of the slice partials
@@ -491,8 +492,8 @@ int mo_muon_plan_step(mo_muon_plan plan, cudaStream_t stream) {
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->dev) return MO_ERR_BAD_PARAM;
   const mo::MuonLayout& L = plan->L;
-  // the prologue's counters and flags start from zero (a per-call upload
-  // would have reset them; a step that gave up may have left them set)
+  // the prologue's counters and flags and the Newton-Schulz tile counters
+  // start from zero (a per-call upload would have reset them)
   cudaError_t e = cudaMemsetAsync(plan->ws + L.off_counters, 0, L.off_lr - L.off_counters, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return mo::enqueue_muon(L, plan->ws, &plan->params, reinterpret_cast<const float*>(plan->ws + L.off_lr), dev,

@@ -19,12 +19,16 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
 // Waits for the phase of `bar` with the given parity. Gives up (returns
 // false) when *abort is set by another role, or when the deadline passes, in
 // which case it sets *abort and records MO_ERR_DEVICE_TIMEOUT in *status.
+// With kCluster the wait acquires at cluster scope (the phase was completed
+// by another CTA of the cluster after storing into this CTA's shared memory).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   int* status, uint64_t timeout_ns) {
-  if (ptx::mbar_test(bar, parity)) return true;
+  auto test = [&] { return kCluster ? ptx::mbar_test_cluster(bar, parity) : ptx::mbar_test(bar, parity); };
+  if (test()) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1; it != 0u; ++it) {
-    if (ptx::mbar_test(bar, parity)) return true;
+    if (test()) return true;
     if ((it & 127u) == 0u) {
       if (*abort) return false;
       if (ptx::globaltimer_ns() - t0 > timeout_ns) break;

@@ -27,6 +27,8 @@ constexpr int kCastTC = 128;
 // Supported maximum sizes (the A and B buffers are m x m).
 constexpr int64_t kMaxDim = int64_t(1) << 22;   // rows or cols
 constexpr int64_t kMaxM = 65536;                 // min(rows, cols)
+constexpr int kMaxNsSteps = 100;                 // Newton-Schulz iterations per step
+constexpr int kMaxNsLaunches = 3 * kMaxNsSteps;  // three grouped GEMM launches per iteration
 
 // Gram products longer than this along their reduction (n) are split into
 // slices of this many columns: each slice accumulates its own fp32 partial

@@ -11,7 +11,9 @@
 // X0 = bf16(V / (||V||_F + eps)) is written by the prologue.
 //
 // Kernel structure: persistent clusters of two CTAs on two SMs (tcgen05
-// cta_group::2), 256 x 256 output tiles, 10 warps per CTA:
+// cta_group::2), 256 x 256 output tiles taken in list order from a counter
+// per launch (the even CTA takes them and shares them with its peer through
+// a ring in shared memory), 10 warps per CTA:
 //   warp 0      TMA producer: this CTA's 128-row halves of the A and B
 //               operands in 64 x 64 boxes (128-byte swizzle) into a 6-stage
 //               shared-memory ring; completion counted on the even CTA's
@@ -302,9 +304,14 @@ __device__ __forceinline__ void epilogue_update(const NsParams& p, const DevMat&
 constexpr int kPairStages = 6;
 constexpr uint32_t kPairHalfBytes = 128 * kBK * 2;                  // 16 KB
 constexpr uint32_t kPairStageBytes = 2 * kPairHalfBytes;            // A half + B half
-constexpr uint32_t kPairNumBars = 2 * kPairStages + 5;
-constexpr uint32_t kPairCtrlBytes = 256;   // barriers; TMEM slot, abort flag, the peer's report (2 words)
-static_assert(8 * kPairNumBars + 16 <= kPairCtrlBytes, "control block");
+constexpr int kSchedSlots = 16;            // ring of published tile numbers
+constexpr int kSchedAhead = 3;             // tiles published ahead of the one the producers load
+constexpr uint32_t kSchedConsumers = 1 + kEpiWarps + 1 + kEpiWarps;   // MMA + epilogues, peer producer + epilogues
+constexpr uint32_t kPairNumBars = 2 * kPairStages + 5 + 2 * kSchedSlots;
+// barriers; TMEM slot, abort flag, the peer's report (2 words); the tile ring
+constexpr uint32_t kPairCtrlBytes = 512;
+static_assert(8 * kPairNumBars + 16 + 4 * kSchedSlots <= kPairCtrlBytes, "control block");
+static_assert(kSchedAhead >= 1 && kSchedAhead < kSchedSlots, "a slot is republished only after its tile was loaded");
 constexpr size_t kPairSmem = 1024 + size_t(kPairStages) * kPairStageBytes + kPairCtrlBytes;
 
 template <int PHASE, bool LAST>
@@ -321,18 +328,20 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // written by the peer CTA at the end: [0] it gave up, [1] its producer's issued stage count
   volatile uint32_t* peer_report = tmem_slot + 2;
+  // tile numbers in launch order, written into both CTAs by the even CTA's producer
+  volatile uint32_t* sched_tile = tmem_slot + 4;
   auto full_bar = [&](int s) { return bars + 8u * uint32_t(s); };
   auto empty_bar = [&](int s) { return bars + 8u * uint32_t(kPairStages + s); };
   auto tfull_bar = [&](int s) { return bars + 8u * uint32_t(2 * kPairStages + s); };
   auto tempty_bar = [&](int s) { return bars + 8u * uint32_t(2 * kPairStages + 2 + s); };
   const uint32_t drain_bar = bars + 8u * uint32_t(2 * kPairStages + 4);
+  auto sfull_bar = [&](int s) { return bars + 8u * uint32_t(2 * kPairStages + 5 + s); };
+  auto sempty_bar = [&](int s) { return bars + 8u * uint32_t(2 * kPairStages + 5 + kSchedSlots + s); };
 
   const int warp = int(threadIdx.x >> 5);
   const int lane = int(threadIdx.x & 31);
   const uint32_t rank = ptx::cluster_ctarank();
   const bool leader = rank == 0;
-  const int cid = int(ptx::cluster_id_x());
-  const int ncl = int(ptx::nclusters_x());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
@@ -344,6 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
       ptx::mbar_init(tempty_bar(s), 2 * kEpiWarps);
     }
     ptx::mbar_init(drain_bar, 1);
+    for (int s = 0; s < kSchedSlots; ++s) {
+      ptx::mbar_init(sfull_bar(s), 1);
+      ptx::mbar_init(sempty_bar(s), kSchedConsumers);
+    }
     *abort_flag = 0;
     peer_report[0] = 0u;
     peer_report[1] = 0u;
@@ -363,6 +376,44 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
+  // Tile schedule: the CTA pairs take the launch's tiles in list order from
+  // one counter, so the pairs work on neighbouring tiles (shared operand
+  // panels stay in L2) and finish within a tile or two of each other. The
+  // even CTA's producer takes the tile numbers and publishes each in a ring
+  // of kSchedSlots slots in both CTAs, kSchedAhead tiles before the
+  // producers load it; every other role reads it there, and a number >=
+  // ntiles ends the role's loop. The even CTA's own roles synchronise on
+  // the ring at CTA scope, the odd CTA's at cluster scope.
+  const uint32_t ntiles = uint32_t(p.ntiles);
+  int sslot = 0;
+  uint32_t sph = 0;
+  // Takes the next published tile number (a consumer role: the MMA issuer,
+  // an epilogue warp, the odd CTA's producer): waits for the slot, reads it,
+  // and releases the slot to the even CTA's producer. One lane per warp.
+  auto next_tile = [&](uint32_t& t) -> bool {
+    bool ok = true;
+    if (lane == 0) {
+      ok = leader ? mbar_wait_bounded<false>(sfull_bar(sslot), sph, abort_flag, p.status, p.timeout_ns)
+                  : mbar_wait_bounded<true>(sfull_bar(sslot), sph, abort_flag, p.status, p.timeout_ns);
+      if (ok) {
+        t = sched_tile[sslot];
+        if (leader)
+          ptx::mbar_arrive(sempty_bar(sslot));
+        else
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(sempty_bar(sslot), 0));
+      }
+    }
+    if (warp >= 2) {
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      t = __shfl_sync(0xFFFFFFFFu, t, 0);
+    }
+    if (++sslot == kSchedSlots) {
+      sslot = 0;
+      sph ^= 1u;
+    }
+    return ok;
+  };
+
   uint32_t n_issued = 0;      // producer: operand stages issued (stage j % S, phase parity (j / S) & 1)
   bool mma_issued = false;    // MMA issuer: any MMA issued
   if (warp == 0) {
@@ -372,7 +423,45 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
       uint32_t ph = 0;
       bool ok = true;
       uint32_t last_mat = 0xFFFFFFFFu;
-      for (int t = cid; ok && t < p.ntiles; t += ncl) {
+      // even CTA: the publishing position in the ring, and the next tile
+      // number, taken from the counter one publication early
+      int pslot = 0;
+      uint32_t pph = 0;
+      bool published_end = false;
+      uint32_t ahead = leader ? atomicAdd(p.tile_ctr, 1u) : 0u;
+      auto publish = [&]() -> bool {
+        if (published_end) return true;
+        if (!mbar_wait_bounded<true>(sempty_bar(pslot), pph ^ 1u, abort_flag, p.status, p.timeout_ns))
+          return false;
+        const uint32_t v = ahead;
+        sched_tile[pslot] = v;
+        ptx::mbar_arrive(sfull_bar(pslot));
+        ptx::st_shared_cluster_u32(ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t*>(sched_tile + pslot)), 1u), v);
+        ptx::mbar_arrive_cluster(ptx::mapa_shared(sfull_bar(pslot), 1u));
+        if (++pslot == kSchedSlots) {
+          pslot = 0;
+          pph ^= 1u;
+        }
+        if (v >= ntiles)
+          published_end = true;
+        else
+          ahead = atomicAdd(p.tile_ctr, 1u);
+        return true;
+      };
+      if (leader)
+        for (int i = 0; ok && i < kSchedAhead; ++i) ok = publish();
+      while (ok) {
+        uint32_t t;
+        if (leader) {
+          // this thread published the slot itself; it is republished only
+          // kSchedSlots - kSchedAhead tiles after this read
+          t = sched_tile[sslot];
+          if (++sslot == kSchedSlots) sslot = 0;
+          if (t < ntiles && !publish()) break;
+        } else if (!next_tile(t)) {
+          break;
+        }
+        if (t >= ntiles) break;
         const TileRec tr = p.tiles[t];
         const DevMat& M = p.mats[tr.mat];
         const CUtensorMap* maps = p.tmaps + size_t(tr.mat) * kMapsPerMat;
@@ -443,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
       int acc = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (int t = cid; ok && t < p.ntiles; t += ncl) {
+      uint32_t t;
+      while (ok && next_tile(t) && t < ntiles) {
         const TileRec tr = p.tiles[t];
         const DevMat& M = p.mats[tr.mat];
         const int K = (PHASE == MO_PHASE_GRAM) ? M.n : M.m;
@@ -487,7 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
     const int r_in = quarter * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
-    for (int t = cid; t < p.ntiles; t += ncl) {
+    uint32_t t;
+    while (next_tile(t) && t < ntiles) {
       const TileRec tr = p.tiles[t];
       const DevMat& M = p.mats[tr.mat];
       if (LAST) prefetch_w_rows(M, int(tr.tm) * 256 + int(rank) * 128 + r_in, int(tr.tn) * kBN + half * kEpiCols);

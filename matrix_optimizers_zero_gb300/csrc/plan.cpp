@@ -63,7 +63,7 @@ int validate_muon_params(const mo_muon_params* p) {
       !finite(p->c) || !finite(p->eps))
     return MO_ERR_BAD_PARAM;
   if (p->eps < 0.f) return MO_ERR_BAD_PARAM;
-  if (p->ns_steps < 1 || p->ns_steps > 100) return MO_ERR_BAD_PARAM;
+  if (p->ns_steps < 1 || p->ns_steps > kMaxNsSteps) return MO_ERR_BAD_PARAM;
   if (p->ns_form != MO_NS_GRAM && p->ns_form != MO_NS_APPENDIX) return MO_ERR_BAD_PARAM;
   if (p->lr_adjust != MO_LR_ORIGINAL && p->lr_adjust != MO_LR_MATCH_RMS_ADAMW) return MO_ERR_BAD_PARAM;
   if (p->nesterov != 0 && p->nesterov != 1) return MO_ERR_BAD_PARAM;
@@ -270,6 +270,8 @@ void plan_muon(const mo_matrix* tbl, int32_t n, int bm, int ns_form, MuonLayout&
   off = align_up(off + sizeof(uint32_t) * size_t(n), 256);
   L.off_abort = off;
   off = align_up(off + sizeof(uint32_t), 256);
+  L.off_tile_ctr = off;
+  off = align_up(off + sizeof(uint32_t) * size_t(kMaxNsLaunches), 256);
   L.off_lr = off;
   off = align_up(off + sizeof(float), 256);
   {

@@ -27,6 +27,7 @@ struct MuonLayout {
   int64_t cast_total = 0;
   size_t off_meta = 0, off_tmaps = 0, off_nrm_prefix = 0, off_cast_prefix = 0, off_counters = 0, off_ready = 0,
          off_abort = 0;
+  size_t off_tile_ctr = 0;           // kMaxNsLaunches tile counters, one per Newton-Schulz launch of a step
   size_t off_lr = 0;                 // one fp32: the learning rate a planned step reads (mo_muon_plan)
   size_t off_reduces = 0;
   size_t off_tiles[3] = {0, 0, 0};

@@ -37,6 +37,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
       : "memory");
 }
 
+// One arrival on an mbarrier of this CTA (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Counts `bytes` as arrived on the mbarrier's current phase without a copy
 // (settles a phase whose expected bytes will never be written).
 __device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
@@ -49,6 +54,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+// Same probe with acquire at cluster scope: pairs with an arrive.release.cluster
+// from another CTA of the cluster, so that CTA's earlier shared::cluster
+// stores into this CTA's shared memory are visible after it returns true.
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -220,6 +240,11 @@ __device__ __forceinline__ void cluster_sync() {
 // (shared::cluster address; ordered for the peer by the next cluster barrier)
 __device__ __forceinline__ void st_shared_cluster_v2(uint32_t cluster_addr, uint32_t a, uint32_t b) {
   asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(cluster_addr), "r"(a), "r"(b) : "memory");
+}
+
+// one 32-bit word to the shared memory of any CTA of the cluster
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // arrive on an mbarrier of any CTA of the cluster (release at cluster scope)

@@ -1,6 +1,7 @@
 """Device-side tile coverage: every Newton-Schulz GEMM launch of a step
 executes each output tile of its schedule exactly once on each CTA of the
-pair that computes it. The counting entry point
+pair that computes it (the pairs take tiles from a per-launch device counter,
+reset for every step). The counting entry point
 (muon_owner_step_coverage) runs the same launches as muon_owner_step, so its
 weights and momentum must come out bit-identical to a plain step's."""
 import pytest
@@ -48,3 +49,22 @@ def test_every_tile_once_gpt2l_four_layers():
     host = [(W.cpu(), G.cpu(), V.cpu()) for W, G, V in mats]
     del mats
     check_coverage(host, mo.MuonParams(ns_steps=2))
+
+
+def test_every_tile_once_on_consecutive_steps():
+    """Two steps on one workspace: each step starts its launches' tile
+    counters from zero, so the second step runs every tile again."""
+    host = host_table(RAGGED, 98)
+    params = mo.MuonParams()
+    counted = to_device(host, DEV)
+    plain = to_device(host, DEV)
+    ws = mo.muon_workspace(counted, params, device=DEV)
+    ws2 = mo.muon_workspace(plain, params, device=DEV)
+    for _ in range(2):
+        cov = mo.muon_owner_step_coverage(counted, params, ws)
+        mo.muon_owner_step(plain, params, ws2)
+        torch.cuda.synchronize()
+        assert mo.mo_last_device_error() == 0
+        assert bool((cov == 1).all())
+    for (Wc, _, Vc), (Wp, _, Vp) in zip(counted, plain):
+        assert torch.equal(Wc, Wp) and torch.equal(Vc, Vp)
