@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define MO_ABI_VERSION 3
+#define MO_ABI_VERSION 4
 
 enum mo_status {
   MO_OK = 0,
@@ -301,8 +301,10 @@ typedef struct {
 enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
 
 /* Writes the tile schedule of one phase (in launch order) into out[0..cap)
- * and the tile count into *count. The CTA pairs of a launch take the tiles in
- * this order from one device counter, each pair the next tile as it frees up. Returns MO_OK, or MO_ERR_BAD_SHAPE if cap is
+ * and the tile count into *count. A launch with at least 256 tiles per CTA
+ * pair hands them out in this order from one device counter, each pair taking
+ * the next as it frees up; a shorter launch assigns them statically (pair c of
+ * P runs tiles c, c + P, c + 2P, ...). Returns MO_OK, or MO_ERR_BAD_SHAPE if cap is
  * too small (then *count holds the required size). Tiles are sorted by
  * decreasing reduction length K (n for the Gram, m otherwise), ties broken by
  * table index, then tile row and tile column (Gram, A.A) or tile column and
@@ -316,8 +318,18 @@ enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
 int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase,
                           mo_tile* out, int64_t cap, int64_t* count);
 
+/* Tile schedule of the Newton-Schulz launches (muon_owner_step_coverage). */
+enum mo_ns_schedule {
+  MO_SCHED_AUTO = 0,     /* as muon_owner_step: by tiles per CTA pair */
+  MO_SCHED_STATIC = 1,   /* every launch assigns its tiles statically */
+  MO_SCHED_COUNTER = 2   /* every launch hands out its tiles from its counter */
+};
+
 /* Test support (no counterpart on the pages): muon_owner_step that also
- * counts on the device how often each Newton-Schulz output tile was executed.
+ * counts on the device how often each Newton-Schulz output tile was executed,
+ * under the tile schedule `schedule` (mo_ns_schedule; MO_ERR_BAD_PARAM for
+ * another value). Every tile's arithmetic is the same under either schedule,
+ * so the results are too, bit for bit.
  *  - *needed (must not be NULL) receives the number of uint32 counters: two
  *    per tile (the even and the odd CTA of the pair that computes it) for
  *    every GEMM launch of the step, in launch order (per iteration: Gram,
@@ -332,7 +344,7 @@ int mo_muon_tile_schedule(const mo_matrix* tbl, int32_t n, int32_t phase,
  * Other arguments and status codes as muon_owner_step. */
 int muon_owner_step_coverage(const mo_matrix* tbl, int32_t n, const mo_muon_params* params,
                              void* ws, size_t ws_bytes, uint32_t* coverage, int64_t coverage_len,
-                             int64_t* needed, cudaStream_t stream);
+                             int32_t schedule, int64_t* needed, cudaStream_t stream);
 
 /* ---- owner planning ("MatrixFSDP", section 4.1, Algorithm 1) ----
  * A role is one 2D matrix or the packed non-matrix tail of one block. The

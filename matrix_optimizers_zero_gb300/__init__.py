@@ -134,7 +134,7 @@ def load_library() -> ctypes.CDLL:
         "mo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "mo_abi_version": (ctypes.c_int, []),
         "mo_muon_tile_schedule": (ctypes.c_int, [P, I32, I32, P, I64, P]),
-        "muon_owner_step_coverage": (ctypes.c_int, [P, I32, P, P, SZ, P, I64, P, P]),
+        "muon_owner_step_coverage": (ctypes.c_int, [P, I32, P, P, SZ, P, I64, I32, P, P]),
         "mo_selftest_bounded_wait": (ctypes.c_int, [I64, P]),
         "muon_owner_step_noalloc": (ctypes.c_int, [P, I32, P, P]),
         "mo_plan_owners": (ctypes.c_int, [P, I32, I32, I32, I64, P, P, P]),
@@ -417,20 +417,25 @@ def fake_table(shapes: Sequence[Tuple[int, int]]):
     return arr
 
 
-def muon_owner_step_coverage(mats, params, workspace, stream=None):
+NS_SCHEDULES = {"auto": 0, "static": 1, "counter": 2}  # mo_ns_schedule
+
+
+def muon_owner_step_coverage(mats, params, workspace, stream=None, schedule="auto"):
     """muon_owner_step that also returns the per-tile execution counters
     (a uint32 device tensor: two per tile of every GEMM launch; all ones when
-    each tile ran exactly once on each CTA of its pair). For tests."""
+    each tile ran exactly once on each CTA of its pair), under the tile
+    schedule named by `schedule` (NS_SCHEDULES). For tests."""
     import torch
     t = _as_table(mats)
     lib = load_library()
+    sched = NS_SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
     needed = ctypes.c_int64(0)
-    _check(lib.muon_owner_step_coverage(t.ptr, t.n, ctypes.byref(params), None, 0, None, 0, ctypes.byref(needed),
-                                        None), "muon_owner_step_coverage")
+    _check(lib.muon_owner_step_coverage(t.ptr, t.n, ctypes.byref(params), None, 0, None, 0, sched,
+                                        ctypes.byref(needed), None), "muon_owner_step_coverage")
     cov = torch.zeros(max(1, needed.value), dtype=torch.int32, device=workspace.device)
     st = lib.muon_owner_step_coverage(t.ptr, t.n, ctypes.byref(params), workspace.data_ptr(),
                                       workspace.numel() * workspace.element_size(), cov.data_ptr(), needed.value,
-                                      ctypes.byref(needed), _stream_ptr(stream))
+                                      sched, ctypes.byref(needed), _stream_ptr(stream))
     _check(st, "muon_owner_step_coverage")
     return cov[:needed.value]
 

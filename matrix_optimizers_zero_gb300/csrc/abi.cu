@@ -179,7 +179,7 @@ namespace mo {
 
 int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* prm, const float* lr_dev,
                  DeviceInfo* dev, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end,
-                 uint32_t* coverage);
+                 const StepHooks* hooks);
 
 // Tile-execution counters of one step (muon_owner_step_coverage): two per
 // tile of every Newton-Schulz GEMM launch, launches in order.
@@ -191,7 +191,7 @@ int64_t coverage_counters(const mo::MuonLayout& L, const mo_muon_params* prm) {
 
 int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* ws, size_t ws_bytes,
                    cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end, bool allow_pinned,
-                   uint32_t* coverage, int64_t coverage_len) {
+                   const StepHooks* hooks) {
   int st = mo::validate_muon_params(prm);
   if (st != MO_OK) return st;
   if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
@@ -217,7 +217,8 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
     delete fresh;
     return MO_ERR_WORKSPACE_TOO_SMALL;
   }
-  if (coverage != nullptr && coverage_len < coverage_counters(E ? E->L : fresh->L, prm)) {
+  if (hooks != nullptr && hooks->coverage != nullptr &&
+      hooks->coverage_len < coverage_counters(E ? E->L : fresh->L, prm)) {
     delete fresh;
     return MO_ERR_BAD_SHAPE;
   }
@@ -252,15 +253,17 @@ int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, v
   if (e != cudaSuccess) return cuda_fail(e);
   if (use_pinned && (e = cudaEventRecord(E->uploaded, stream)) != cudaSuccess) return cuda_fail(e);
 
-  return enqueue_muon(L, wsb, prm, nullptr, dev, stream, ev_begin, ev_end, coverage);
+  return enqueue_muon(L, wsb, prm, nullptr, dev, stream, ev_begin, ev_end, hooks);
 }
 
 // The prologue and Newton-Schulz launches of one step whose workspace header
 // is in place; the learning rate comes from `lr_dev` when it is set.
 int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* prm, const float* lr_dev,
                  DeviceInfo* dev, cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end,
-                 uint32_t* coverage) {
+                 const StepHooks* hooks) {
   cudaError_t e;
+  uint32_t* coverage = hooks ? hooks->coverage : nullptr;
+  const int32_t schedule = hooks ? hooks->schedule : MO_SCHED_AUTO;
   const mo::DevMat* d_mats = reinterpret_cast<const mo::DevMat*>(wsb + L.off_meta);
   float* d_scales = reinterpret_cast<float*>(wsb + L.off_scales);
 
@@ -312,6 +315,9 @@ int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* pr
       np.coverage = coverage;
       if (coverage != nullptr) coverage += 2 * size_t(np.ntiles);
       np.tile_ctr = reinterpret_cast<uint32_t*>(wsb + L.off_tile_ctr) + (3 * it + k);
+      np.counter_tiles = schedule == MO_SCHED_COUNTER ? 1
+                         : schedule == MO_SCHED_STATIC ? 0
+                         : (int64_t(np.ntiles) >= mo::kCounterTilesPerPair * int64_t(grid / 2) ? 1 : 0);
       if ((e = mo::launch_ns_phase(kinds[k], last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
       if (k == 0 && L.reduce_blocks > 0) {
         // long matrices: A = sum of the slice partials
@@ -520,18 +526,20 @@ size_t mo_muon_workspace_bytes(const mo_matrix* tbl, int32_t n, const mo_muon_pa
 
 int muon_owner_step(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws, size_t ws_bytes,
                     cudaStream_t stream) {
-  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr, true, nullptr, 0);
+  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr, true, nullptr);
 }
 
 int muon_owner_step_timed(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws,
                           size_t ws_bytes, cudaStream_t stream, cudaEvent_t ev_ns_begin, cudaEvent_t ev_ns_end) {
-  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, ev_ns_begin, ev_ns_end, true, nullptr, 0);
+  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, ev_ns_begin, ev_ns_end, true, nullptr);
 }
 
 int muon_owner_step_coverage(const mo_matrix* tbl, int32_t n, const mo_muon_params* params, void* ws,
-                             size_t ws_bytes, uint32_t* coverage, int64_t coverage_len, int64_t* needed,
-                             cudaStream_t stream) {
+                             size_t ws_bytes, uint32_t* coverage, int64_t coverage_len, int32_t schedule,
+                             int64_t* needed, cudaStream_t stream) {
   if (!needed) return MO_ERR_NULL_POINTER;
+  if (schedule != MO_SCHED_AUTO && schedule != MO_SCHED_STATIC && schedule != MO_SCHED_COUNTER)
+    return MO_ERR_BAD_PARAM;
   int st = mo::validate_muon_params(params);
   if (st != MO_OK) return st;
   if ((st = mo::validate_matrix_table(tbl, n)) != MO_OK) return st;
@@ -543,7 +551,8 @@ int muon_owner_step_coverage(const mo_matrix* tbl, int32_t n, const mo_muon_para
   mo::plan_muon(tbl, n, mo::kBM, params->ns_form, L);
   *needed = mo::coverage_counters(L, params);
   if (coverage == nullptr) return MO_OK;   // size query
-  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr, true, coverage, coverage_len);
+  const mo::StepHooks hooks{coverage, coverage_len, schedule};
+  return mo::muon_step_impl(tbl, n, params, ws, ws_bytes, stream, nullptr, nullptr, true, &hooks);
 }
 
 int rmnp_step(const mo_matrix* tbl, int32_t n, const mo_rmnp_params* params, cudaStream_t stream) {

@@ -25,7 +25,8 @@ struct NsParams {
   int32_t lr_adjust;          // mo_lr_adjust: which per-matrix scale the update uses
   uint64_t timeout_ns;
   uint32_t* coverage;         // tests only (null otherwise): per tile, two execution counters (even, odd CTA)
-  uint32_t* tile_ctr;         // this launch's tile counter (zero on entry): CTA pairs take tiles in list order
+  uint32_t* tile_ctr;         // this launch's tile counter (zero on entry)
+  int32_t counter_tiles;      // 1: CTA pairs take tiles in list order from tile_ctr; 0: pair c runs c, c + pairs, ...
 };
 
 // 256 x 256 tiles on CTA pairs; grid must be even (two CTAs per cluster).

@@ -30,6 +30,21 @@ constexpr int64_t kMaxM = 65536;                 // min(rows, cols)
 constexpr int kMaxNsSteps = 100;                 // Newton-Schulz iterations per step
 constexpr int kMaxNsLaunches = 3 * kMaxNsSteps;  // three grouped GEMM launches per iteration
 
+// A Newton-Schulz launch with at least this many tiles per CTA pair takes its
+// tiles from a device counter; shorter ones assign them statically (pair c
+// runs tiles c, c + pairs, ...). Over a long launch the static assignment
+// lets the pairs drift apart until the tiles in flight span more operand
+// panels than L2 holds; on short launches it is the faster of the two.
+constexpr int64_t kCounterTilesPerPair = 256;
+
+// Test support of muon_owner_step_coverage: per-tile execution counters and a
+// forced tile schedule (mo_ns_schedule).
+struct StepHooks {
+  uint32_t* coverage;
+  int64_t coverage_len;
+  int32_t schedule;
+};
+
 // Gram products longer than this along their reduction (n) are split into
 // slices of this many columns: each slice accumulates its own fp32 partial
 // (tcgen05 accumulation over very long reductions drops products far below

@@ -11,9 +11,10 @@
 // X0 = bf16(V / (||V||_F + eps)) is written by the prologue.
 //
 // Kernel structure: persistent clusters of two CTAs on two SMs (tcgen05
-// cta_group::2), 256 x 256 output tiles taken in list order from a counter
-// per launch (the even CTA takes them and shares them with its peer through
-// a ring in shared memory), 10 warps per CTA:
+// cta_group::2), 256 x 256 output tiles, taken in list order from a counter
+// per launch on long launches (the even CTA takes them and shares them with
+// its peer through a ring in shared memory) and assigned statically on short
+// ones, 10 warps per CTA:
 //   warp 0      TMA producer: this CTA's 128-row halves of the A and B
 //               operands in 64 x 64 boxes (128-byte swizzle) into a 6-stage
 //               shared-memory ring; completion counted on the even CTA's
@@ -314,7 +315,9 @@ static_assert(8 * kPairNumBars + 16 + 4 * kSchedSlots <= kPairCtrlBytes, "contro
 static_assert(kSchedAhead >= 1 && kSchedAhead < kSchedSlots, "a slot is republished only after its tile was loaded");
 constexpr size_t kPairSmem = 1024 + size_t(kPairStages) * kPairStageBytes + kPairCtrlBytes;
 
-template <int PHASE, bool LAST>
+// COUNTER: the tile schedule (p.counter_tiles), compiled separately so that
+// neither variant carries the other's branches.
+template <int PHASE, bool LAST, bool COUNTER>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_constant__ NsParams p) {
   // m x n outputs (B operand X or A X, MN-major, K = m) vs symmetric m x m ones
   constexpr bool kWide = PHASE == MO_PHASE_UPDATE || PHASE == kPhaseAX || PHASE == kPhaseABX;
@@ -376,21 +379,31 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
-  // Tile schedule: the CTA pairs take the launch's tiles in list order from
-  // one counter, so the pairs work on neighbouring tiles (shared operand
-  // panels stay in L2) and finish within a tile or two of each other. The
-  // even CTA's producer takes the tile numbers and publishes each in a ring
-  // of kSchedSlots slots in both CTAs, kSchedAhead tiles before the
-  // producers load it; every other role reads it there, and a number >=
-  // ntiles ends the role's loop. The even CTA's own roles synchronise on
-  // the ring at CTA scope, the odd CTA's at cluster scope.
+  // Tile schedule. With COUNTER the CTA pairs take the launch's
+  // tiles in list order from one counter, so the pairs work on neighbouring
+  // tiles (shared operand panels stay in L2) and finish within a tile or two
+  // of each other. The even CTA's producer takes the tile numbers and
+  // publishes each in a ring of kSchedSlots slots in both CTAs, kSchedAhead
+  // tiles before the producers load it; every other role reads it there,
+  // and a number >= ntiles ends the role's loop. The even CTA's own roles
+  // synchronise on the ring at CTA scope, the odd CTA's at cluster scope.
+  // Without it every role of pair c runs tiles c, c + pairs, ... by itself.
   const uint32_t ntiles = uint32_t(p.ntiles);
+  constexpr bool by_counter = COUNTER;
+  uint32_t static_next = ptx::cluster_id_x();
+  const uint32_t npairs = ptx::nclusters_x();
   int sslot = 0;
   uint32_t sph = 0;
-  // Takes the next published tile number (a consumer role: the MMA issuer,
-  // an epilogue warp, the odd CTA's producer): waits for the slot, reads it,
-  // and releases the slot to the even CTA's producer. One lane per warp.
+  // Takes the next tile number (a consumer role: the MMA issuer, an
+  // epilogue warp, the odd CTA's producer; with the static schedule every
+  // role). From the ring: waits for the slot, reads it, and releases the
+  // slot to the even CTA's producer, one lane per warp.
   auto next_tile = [&](uint32_t& t) -> bool {
+    if (!by_counter) {
+      t = static_next;
+      static_next += npairs;
+      return true;
+    }
     bool ok = true;
     if (lane == 0) {
       ok = leader ? mbar_wait_bounded<false>(sfull_bar(sslot), sph, abort_flag, p.status, p.timeout_ns)
@@ -428,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
       int pslot = 0;
       uint32_t pph = 0;
       bool published_end = false;
-      uint32_t ahead = leader ? atomicAdd(p.tile_ctr, 1u) : 0u;
+      const bool publisher = leader && by_counter;
+      uint32_t ahead = publisher ? atomicAdd(p.tile_ctr, 1u) : 0u;
       auto publish = [&]() -> bool {
         if (published_end) return true;
         if (!mbar_wait_bounded<true>(sempty_bar(pslot), pph ^ 1u, abort_flag, p.status, p.timeout_ns))
@@ -448,11 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
           ahead = atomicAdd(p.tile_ctr, 1u);
         return true;
       };
-      if (leader)
+      if (publisher)
         for (int i = 0; ok && i < kSchedAhead; ++i) ok = publish();
       while (ok) {
         uint32_t t;
-        if (leader) {
+        if (publisher) {
           // this thread published the slot itself; it is republished only
           // kSchedSlots - kSchedAhead tiles after this read
           t = sched_tile[sslot];
@@ -734,7 +748,7 @@ __global__ void bounded_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 
 template <int PHASE, bool LAST>
 cudaError_t launch_pair(const NsParams& p, int grid, cudaStream_t stream) {
-  auto kern = ns_gemm_pair_kernel<PHASE, LAST>;
+  auto kern = p.counter_tiles != 0 ? ns_gemm_pair_kernel<PHASE, LAST, true> : ns_gemm_pair_kernel<PHASE, LAST, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kPairSmem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

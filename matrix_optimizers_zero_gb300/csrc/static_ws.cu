@@ -21,12 +21,13 @@
 #include "mo.h"
 
 namespace mo {
+struct StepHooks;
 void note_cuda_error(int e);   // records the code returned by mo_last_cuda_error()
 // The Muon step of abi.cu; allow_pinned = false keeps every host upload in
 // pageable memory, so this path allocates no pinned or device memory.
 int muon_step_impl(const mo_matrix* tbl, int32_t n, const mo_muon_params* prm, void* ws, size_t ws_bytes,
                    cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end, bool allow_pinned,
-                   uint32_t* coverage, int64_t coverage_len);
+                   const StepHooks* hooks);
 }
 
 namespace {
@@ -90,8 +91,7 @@ int muon_owner_step_noalloc(const mo_matrix* tbl, int32_t n, const mo_muon_param
   if (st != MO_OK) return st;
   // The per-call header written at the start of the scratch resets every
   // counter the step relies on; all other scratch is written before it is read.
-  return mo::muon_step_impl(tbl, n, params, scratch, kStaticScratchBytes, stream, nullptr, nullptr, false, nullptr,
-                            0);
+  return mo::muon_step_impl(tbl, n, params, scratch, kStaticScratchBytes, stream, nullptr, nullptr, false, nullptr);
 }
 
 }  // extern "C"

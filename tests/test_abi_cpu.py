@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
     assert len(names) >= 12
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.mo_abi_version() == 3
+    assert lib.mo_abi_version() == 4
 
 
 def test_status_strings(lib):
@@ -308,13 +308,18 @@ def test_tile_coverage_size_query(lib):
         p = mo.MuonParams(ns_form=form, ns_steps=steps)
         arr = mo.fake_table(shapes)
         need = ctypes.c_int64(-1)
-        st = lib.muon_owner_step_coverage(ctypes.cast(arr, ctypes.c_void_p), len(shapes), ctypes.byref(p), None, 0,
-                                          None, 0, ctypes.byref(need), None)
-        assert st == 0
-        mid = 1 if form == "gram" else 2
-        per_iter = sum(len(mo.mo_muon_tile_schedule(shapes, ph)) for ph in (0, mid, 2))
-        assert need.value == 2 * steps * per_iter
-    # a null count pointer is rejected before anything else
+        for sched in (0, 1, 2):
+            st = lib.muon_owner_step_coverage(ctypes.cast(arr, ctypes.c_void_p), len(shapes), ctypes.byref(p), None,
+                                              0, None, 0, sched, ctypes.byref(need), None)
+            assert st == 0
+            mid = 1 if form == "gram" else 2
+            per_iter = sum(len(mo.mo_muon_tile_schedule(shapes, ph)) for ph in (0, mid, 2))
+            assert need.value == 2 * steps * per_iter
+    # a null count pointer is rejected before anything else, then an unknown schedule
     arr = mo.fake_table([(16, 32)])
     assert lib.muon_owner_step_coverage(ctypes.cast(arr, ctypes.c_void_p), 1, ctypes.byref(mo.MuonParams()), None, 0,
-                                        None, 0, None, None) == -1
+                                        None, 0, 0, None, None) == -1
+    need = ctypes.c_int64(-1)
+    for bad in (-1, 3):
+        assert lib.muon_owner_step_coverage(ctypes.cast(arr, ctypes.c_void_p), 1, ctypes.byref(mo.MuonParams()),
+                                            None, 0, None, 0, bad, ctypes.byref(need), None) == -4

@@ -1,9 +1,11 @@
 """Device-side tile coverage: every Newton-Schulz GEMM launch of a step
 executes each output tile of its schedule exactly once on each CTA of the
-pair that computes it (the pairs take tiles from a per-launch device counter,
-reset for every step). The counting entry point
-(muon_owner_step_coverage) runs the same launches as muon_owner_step, so its
-weights and momentum must come out bit-identical to a plain step's."""
+pair that computes it, under both tile schedules: static (pair c runs tiles
+c, c + pairs, ...) and from a per-launch device counter (reset for every
+step). The counting entry point (muon_owner_step_coverage) runs the same
+launches as muon_owner_step, and a tile's arithmetic does not depend on which
+pair runs it or when, so its weights and momentum must come out bit-identical
+to a plain step's (which uses the static schedule on these tables)."""
 import pytest
 import torch
 
@@ -22,11 +24,11 @@ def host_table(shapes, config_id):
     return [workloads.host_matrix(wl, i, v_std=1e-3) for i in range(len(shapes))]
 
 
-def check_coverage(host, params):
+def check_coverage(host, params, schedule):
     counted = to_device(host, DEV)
     plain = to_device(host, DEV)
     ws = mo.muon_workspace(counted, params, device=DEV)
-    cov = mo.muon_owner_step_coverage(counted, params, ws)
+    cov = mo.muon_owner_step_coverage(counted, params, ws, schedule=schedule)
     ws2 = mo.muon_workspace(plain, params, device=DEV)
     mo.muon_owner_step(plain, params, ws2)
     torch.cuda.synchronize()
@@ -38,22 +40,25 @@ def check_coverage(host, params):
         assert torch.equal(Wc, Wp) and torch.equal(Vc, Vp)
 
 
+@pytest.mark.parametrize("schedule", ["static", "counter"])
 @pytest.mark.parametrize("form", ["gram", "appendix"])
-def test_every_tile_once_ragged_table(form):
-    check_coverage(host_table(RAGGED, 97), mo.MuonParams(ns_form=form))
+def test_every_tile_once_ragged_table(form, schedule):
+    check_coverage(host_table(RAGGED, 97), mo.MuonParams(ns_form=form), schedule)
 
 
-def test_every_tile_once_gpt2l_four_layers():
+@pytest.mark.parametrize("schedule", ["static", "counter"])
+def test_every_tile_once_gpt2l_four_layers(schedule):
     wl = workloads.get_workload("gpt2l_4layers")
     mats = workloads.device_matrices(wl, DEV, v_std=1e-3)
     host = [(W.cpu(), G.cpu(), V.cpu()) for W, G, V in mats]
     del mats
-    check_coverage(host, mo.MuonParams(ns_steps=2))
+    check_coverage(host, mo.MuonParams(ns_steps=2), schedule)
 
 
 def test_every_tile_once_on_consecutive_steps():
-    """Two steps on one workspace: each step starts its launches' tile
-    counters from zero, so the second step runs every tile again."""
+    """Two steps on one workspace under the counter schedule: each step starts
+    its launches' tile counters from zero, so the second step runs every tile
+    again."""
     host = host_table(RAGGED, 98)
     params = mo.MuonParams()
     counted = to_device(host, DEV)
@@ -61,7 +66,7 @@ def test_every_tile_once_on_consecutive_steps():
     ws = mo.muon_workspace(counted, params, device=DEV)
     ws2 = mo.muon_workspace(plain, params, device=DEV)
     for _ in range(2):
-        cov = mo.muon_owner_step_coverage(counted, params, ws)
+        cov = mo.muon_owner_step_coverage(counted, params, ws, schedule="counter")
         mo.muon_owner_step(plain, params, ws2)
         torch.cuda.synchronize()
         assert mo.mo_last_device_error() == 0
