@@ -608,9 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
         epilogue_update<PHASE, LAST>(p, M, row, cbase, tb);
       else
         epilogue_symmetric<PHASE>(p, M, row, cbase, tb);
+      // hand the accumulator back: its reads are complete (tcgen05.wait::ld)
+      // and fenced; the tile's global stores need no ordering inside the
+      // launch, so the arrive releases at CTA scope and does not wait for them
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+      if (lane == 0) ptx::mbar_arrive_remote_cta(ptx::mapa_shared(tempty_bar(acc), 0));
       if (p.coverage != nullptr && warp == 2 && lane == 0) atomicAdd(p.coverage + 2 * size_t(t) + rank, 1u);
       acc ^= 1;
       if (acc == 0) aph ^= 1u;

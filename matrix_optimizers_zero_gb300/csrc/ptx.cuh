@@ -247,6 +247,14 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// arrive on an mbarrier of any CTA of the cluster, releasing at CTA scope
+// only: it orders nothing of this thread's global memory traffic for the
+// waiter (used where the arrive hands over a TMEM accumulator, whose reads
+// tcgen05.wait::ld and tcgen05.fence::before_thread_sync already ordered)
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // arrive on an mbarrier of any CTA of the cluster (release at cluster scope)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
