@@ -42,15 +42,15 @@ UNIT = "TFLOP/s"
 # Newton-Schulz launches, per workload, from an ncu capture of the named
 # capture workload scaled by `scale` (the capture workload holds 1/scale of
 # the table's matrices). Valid only for the kernel source and tile schedule it
-# was measured on (hash of ns_gemm.cu and plan.cpp); the profiles directory
-# holds the capture summaries with their commands.
+# was measured on (hash of ns_gemm.cu, plan.cpp, abi.cu and mo_internal.h);
+# the profiles directory holds the capture summaries with their commands.
 NS_TRAFFIC = {
-    "llama8b": {"source_sha256_16": "de604d48909ee40b", "bytes_per_ns_segment": 483.992e9,
+    "llama8b": {"source_sha256_16": "6a1c130d49d42275", "bytes_per_ns_segment": 495.157e9,
                 "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
-                       "fourth step on the full table"},
-    "gpt2l": {"source_sha256_16": "de604d48909ee40b", "bytes_per_ns_segment": 34.914e9,
+                       "fourth step on the full table (tiles from the per-launch counter)"},
+    "gpt2l": {"source_sha256_16": "6a1c130d49d42275", "bytes_per_ns_segment": 37.362e9,
               "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
-                     "fourth step on the full table"},
+                     "fourth step on the full table (static tile assignment)"},
 }
 # A timed region at least this long is "a kernel timed inside a long step":
 # its roofline uses the sustained bf16 peak, a shorter one the burst peak.
@@ -79,7 +79,8 @@ def choose_peak(peaks, region_s: float):
 def source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    for name in ("ns_gemm.cu", "plan.cpp"):
+    # the kernel, the tile lists, and the per-launch choice of tile schedule
+    for name in ("ns_gemm.cu", "plan.cpp", "abi.cu", "mo_internal.h"):
         with open(os.path.join(ROOT, "matrix_optimizers_zero_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
