@@ -45,12 +45,12 @@ UNIT = "TFLOP/s"
 # was measured on (hash of ns_gemm.cu, plan.cpp, abi.cu and mo_internal.h);
 # the profiles directory holds the capture summaries with their commands.
 NS_TRAFFIC = {
-    "llama8b": {"source_sha256_16": "6a1c130d49d42275", "bytes_per_ns_segment": 495.157e9,
+    "llama8b": {"source_sha256_16": "1c2e232d0dd7c0f3", "bytes_per_ns_segment": 469.903e9,
                 "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
-                       "fourth step on the full table (tiles from the per-launch counter)"},
-    "gpt2l": {"source_sha256_16": "6a1c130d49d42275", "bytes_per_ns_segment": 37.362e9,
+                       "fourth step on the full table (tiles from the per-launch counter; 470-495 GB over captures)"},
+    "gpt2l": {"source_sha256_16": "1c2e232d0dd7c0f3", "bytes_per_ns_segment": 34.910e9,
               "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
-                     "fourth step on the full table (static tile assignment)"},
+                     "fourth step on the full table (static tile assignment; the last launch from the counter)"},
 }
 # A timed region at least this long is "a kernel timed inside a long step":
 # its roofline uses the sustained bf16 peak, a shorter one the burst peak.

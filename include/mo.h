@@ -302,9 +302,10 @@ enum mo_ns_phase { MO_PHASE_GRAM = 0, MO_PHASE_POLY = 1, MO_PHASE_UPDATE = 2 };
 
 /* Writes the tile schedule of one phase (in launch order) into out[0..cap)
  * and the tile count into *count. A launch with at least 256 tiles per CTA
- * pair hands them out in this order from one device counter, each pair taking
- * the next as it frees up; a shorter launch assigns them statically (pair c of
- * P runs tiles c, c + P, c + 2P, ...). Returns MO_OK, or MO_ERR_BAD_SHAPE if cap is
+ * pair (128 for the last launch, which applies the weight update) hands them
+ * out in this order from one device counter, each pair taking the next as it
+ * frees up; a shorter launch assigns them statically (pair c of P runs tiles
+ * c, c + P, c + 2P, ...). Returns MO_OK, or MO_ERR_BAD_SHAPE if cap is
  * too small (then *count holds the required size). Tiles are sorted by
  * decreasing reduction length K (n for the Gram, m otherwise), ties broken by
  * table index, then tile row and tile column (Gram, A.A) or tile column and

@@ -317,7 +317,9 @@ int enqueue_muon(const mo::MuonLayout& L, uint8_t* wsb, const mo_muon_params* pr
       np.tile_ctr = reinterpret_cast<uint32_t*>(wsb + L.off_tile_ctr) + (3 * it + k);
       np.counter_tiles = schedule == MO_SCHED_COUNTER ? 1
                          : schedule == MO_SCHED_STATIC ? 0
-                         : (int64_t(np.ntiles) >= mo::kCounterTilesPerPair * int64_t(grid / 2) ? 1 : 0);
+                         : (int64_t(np.ntiles) >= (last ? mo::kCounterTilesPerPairLast : mo::kCounterTilesPerPair) *
+                                                         int64_t(grid / 2)
+                                ? 1 : 0);
       if ((e = mo::launch_ns_phase(kinds[k], last, np, grid, stream)) != cudaSuccess) return cuda_fail(e);
       if (k == 0 && L.reduce_blocks > 0) {
         // long matrices: A = sum of the slice partials

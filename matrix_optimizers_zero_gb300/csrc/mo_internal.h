@@ -36,6 +36,11 @@ constexpr int kMaxNsLaunches = 3 * kMaxNsSteps;  // three grouped GEMM launches 
 // lets the pairs drift apart until the tiles in flight span more operand
 // panels than L2 holds; on short launches it is the faster of the two.
 constexpr int64_t kCounterTilesPerPair = 256;
+// The last launch (weight update) streams W through L2 beside its operands;
+// from this many tiles per pair the drifting static assignment lets that
+// stream evict X column panels (measured: +2% reads at 47 tiles per pair, +45%
+// at 142), so it takes the counter earlier.
+constexpr int64_t kCounterTilesPerPairLast = 128;
 
 // Test support of muon_owner_step_coverage: per-tile execution counters and a
 // forced tile schedule (mo_ns_schedule).
