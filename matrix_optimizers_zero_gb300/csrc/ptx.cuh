@@ -248,9 +248,11 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
 }
 
 // arrive on an mbarrier of any CTA of the cluster, releasing at CTA scope
-// only: it orders nothing of this thread's global memory traffic for the
-// waiter (used where the arrive hands over a TMEM accumulator, whose reads
-// tcgen05.wait::ld and tcgen05.fence::before_thread_sync already ordered)
+// only: the thread's earlier memory operations are ordered for threads of its
+// own CTA, not for a waiter in another CTA, and the arrive does not wait for
+// its global stores to be acknowledged (used where the arrive hands over a
+// TMEM accumulator, whose reads tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync already ordered)
 __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
