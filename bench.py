@@ -42,13 +42,14 @@ UNIT = "TFLOP/s"
 # Newton-Schulz launches, per workload, from an ncu capture of the named
 # capture workload scaled by `scale` (the capture workload holds 1/scale of
 # the table's matrices). Valid only for the kernel source and tile schedule it
-# was measured on (hash of ns_gemm.cu, plan.cpp, abi.cu and mo_internal.h);
-# the profiles directory holds the capture summaries with their commands.
+# was measured on (hash of ns_gemm.cu, its device helpers, plan.cpp, abi.cu and
+# mo_internal.h); the profiles directory holds the capture summaries with their
+# commands.
 NS_TRAFFIC = {
-    "llama8b": {"source_sha256_16": "1c2e232d0dd7c0f3", "bytes_per_ns_segment": 469.903e9,
+    "llama8b": {"source_sha256_16": "4e806d95c73f9fef", "bytes_per_ns_segment": 469.903e9,
                 "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
                        "fourth step on the full table (tiles from the per-launch counter; 470-495 GB over captures)"},
-    "gpt2l": {"source_sha256_16": "1c2e232d0dd7c0f3", "bytes_per_ns_segment": 34.910e9,
+    "gpt2l": {"source_sha256_16": "4e806d95c73f9fef", "bytes_per_ns_segment": 34.910e9,
               "how": "ncu dram__bytes_read.sum + dram__bytes_write.sum (one pass) over the 15 NS launches of the "
                      "fourth step on the full table (static tile assignment; the last launch from the counter)"},
 }
@@ -79,8 +80,9 @@ def choose_peak(peaks, region_s: float):
 def source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
-    # the kernel, the tile lists, and the per-launch choice of tile schedule
-    for name in ("ns_gemm.cu", "plan.cpp", "abi.cu", "mo_internal.h"):
+    # the kernel and its device helpers, the tile lists, and the per-launch
+    # choice of tile schedule
+    for name in ("ns_gemm.cu", "ptx.cuh", "device_common.cuh", "plan.cpp", "abi.cu", "mo_internal.h"):
         with open(os.path.join(ROOT, "matrix_optimizers_zero_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
